@@ -1,0 +1,3 @@
+"""fp64 CPU oracle (test infrastructure only; see kd_oracle's docstring)."""
+
+from .kd_oracle import *  # noqa: F401,F403
