@@ -1,0 +1,165 @@
+/*
+ * kd.h - C ABI of libkd: offline top-K knowledge distillation on one B300.
+ *
+ * Two operations, both from the method "Efficient Knowledge Distillation for
+ * LLMs: Offline Top-K Logits and a Fused Chunked KL Loss" as described on
+ * the pages:
+ *   [KD-TH] "ทำให้ Knowledge Distillation มีประสิทธิภาพ คุ้มค่า และใช้งานได้จริงใน
+ *           ระดับ Scale ใหญ่" (ai-thai.com)
+ *   [KD-RU] "Multiverse Computing сократила видеопамять для дистилляции
+ *           нейросетей до 15,6 раза" (iitog.ru)
+ *   [KD-TA] "பெரிய மொழி மாதிரிகளைச் சுருக்குதல்: ஒற்றை GPU-க்குள் நினைவகத்தைக்
+ *           கொண்டு வரும் புதிய முறை" (scitechpulse.com)
+ *
+ *  1. kd_topk_cache: the offline teacher cache. Teacher logits become the K
+ *     most probable token ids per position plus their full-vocabulary
+ *     log-softmax values ([KD-TH] section "การทำ Distillation แบบ Offline";
+ *     [KD-RU] fourth paragraph).
+ *  2. kd_fused_kl_fwd / kd_fused_kl_bwd: the fused chunked KL loss. The
+ *     student's final projection z = H W^T is folded into the loss and
+ *     computed chunk by chunk of positions, so the T x V logit matrix never
+ *     exists. The backward pass recomputes each chunk instead of storing it
+ *     ([KD-TH] section "กลไก Fused Chunked KL Loss", variant "Fused chunked KL";
+ *     [KD-TA] fifth paragraph).
+ *
+ * What is computed (the oracle's definition). Per position t:
+ *   lse_t  = log sum_j exp z_tj over the full vocabulary, z_t = W h_t
+ *   p_tk   = exp(l_tk - log sum_k' exp l_tk')   (teacher renormalised over K)
+ *   L_t    = sum_k p_tk log p_tk - sum_k p_tk z_{t,id_tk} + lse_t
+ *   loss   = (1/T) sum_t L_t
+ *   dz_tj  = s * (exp(z_tj - lse_t) - sum_k p_tk [id_tk == j])
+ *   dH     = dz W,   dW (+)= dz^T H
+ * with s = grad_scale (times *grad_scale_dev when given). For the mean loss,
+ * s = dLoss_total/dloss * (1/T).
+ *
+ * Conventions for every entry point:
+ *  - Pointers are device pointers into memory that the caller owns. The
+ *    library never allocates or frees device memory. The workspace `ws` is
+ *    caller-allocated scratch of at least the size its *_workspace_size query
+ *    returns, aligned to 256 bytes.
+ *  - All matrices are row-major and contiguous unless an `ld` (row stride in
+ *    elements) is given. bf16 is IEEE bfloat16 (1-8-7) stored as uint16.
+ *  - `stream` is a cudaStream_t cast to void*. NULL means the legacy default
+ *    stream. Calls enqueue their work and return without synchronising.
+ *    Calls that share one workspace must not overlap on the GPU.
+ *  - Argument errors come back synchronously, before anything is launched,
+ *    as KD_ERR_INVALID_ARG / KD_ERR_UNSUPPORTED / KD_ERR_WORKSPACE. A failed
+ *    launch returns KD_ERR_CUDA. Errors found on the device are recorded in a
+ *    status word inside `ws`: a cache id outside [0, V), or a pipeline wait
+ *    that gave up after its time limit. The first error wins, and the word
+ *    keeps it until kd_read_device_status reads and clears it.
+ */
+#ifndef KD_H_
+#define KD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KD_API __attribute__((visibility("default")))
+#else
+#define KD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kd_status {
+  KD_OK = 0,
+  KD_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, K > V, bad dtype */
+  KD_ERR_UNSUPPORTED = 2,   /* a size the kernels do not handle (see each call) */
+  KD_ERR_WORKSPACE = 3,     /* ws is NULL, misaligned or smaller than required */
+  KD_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed */
+  KD_ERR_DEVICE_TIMEOUT = 5,/* a device-side wait exceeded its time limit */
+  KD_ERR_BAD_ID = 6         /* a cached id outside [0, V) (that entry was ignored) */
+} kd_status;
+
+typedef enum kd_dtype { KD_BF16 = 0, KD_F32 = 1 } kd_dtype;
+
+/* Human-readable name of a status code. Never NULL. */
+KD_API const char* kd_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+KD_API int kd_version(void);
+
+/* ---------------------------------------------------------------- top-K cache
+ *
+ * kd_topk_cache: teacher logits -> offline top-K cache.
+ *   logits  [T, ld] of `dtype` (KD_BF16 or KD_F32), device. Row t holds V
+ *           logits in its first V entries. ld >= V.
+ *   ids     [T, K] int32, device, written: per row the K ids with the largest
+ *           logits, ordered by value descending and then id ascending. Ties at
+ *           the K-th place therefore go to the lowest ids, and -0.0 ties +0.0.
+ *   logp    [T, K] float32, device, written: x[t, id] - log sum_j exp x[t, j]
+ *           (the full-vocabulary log-softmax at those ids), computed in fp32.
+ *   Requires 1 <= K <= V, V < 2^31, and finite logits. The logits pointer
+ *   needs only element alignment, and any ld is accepted (each row is read
+ *   with 16-byte loads from its first 16-byte boundary). Rows are selected from per-thread
+ *   candidate lists (K <= 2048). A row where that could miss an element
+ *   (heavy ties at the K-th value, or K > 2048) is redone by an exact radix
+ *   selection. Both paths give the same result.
+ *   Workspace: kd_topk_workspace_size(T, V, K, dtype) bytes: the status word,
+ *   then (second int32) a running count of rows that took the radix path.
+ */
+KD_API size_t kd_topk_workspace_size(int64_t T, int64_t V, int32_t K, int32_t dtype);
+KD_API int kd_topk_cache(const void* logits, int32_t dtype, int64_t T, int64_t V, int64_t ld,
+                  int32_t K, int32_t* ids, float* logp, void* ws, size_t ws_bytes,
+                  void* stream);
+
+/* ------------------------------------------------------------ fused KL loss
+ *
+ * Shared arguments:
+ *   H     [T, d] bf16, device: student final hidden states.
+ *   W     [V, d] bf16, device: student LM-head (final projection) weights.
+ *   ids   [T, K] int32 and logp [T, K] float32, device: the teacher cache
+ *         (any order within a row; logp need not be normalised). Ids should
+ *         be distinct within a row. Duplicates are summed, as the scatter-add
+ *         gradient does. An id outside [0, V) is ignored and sets
+ *         KD_ERR_BAD_ID in the status word.
+ *   chunk positions per chunk, 1 <= chunk. The workspace grows as chunk * V;
+ *         the chunk size changes results only by fp32 rounding order.
+ *   Requires d % 8 == 0 (16-byte rows for TMA), 16-byte aligned H and W,
+ *   1 <= K <= 4096, 1 <= V < 2^31.
+ *   Workspace: kd_fused_kl_workspace_size(d, V, K, chunk) bytes. It does not
+ *   depend on T; one workspace serves both calls.
+ */
+KD_API size_t kd_fused_kl_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk);
+
+/* Forward. Writes:
+ *   loss       device float32 scalar: (1/T) sum_t L_t.
+ *   lse        [T] float32 device: log-sum-exp of the student logits per
+ *              position. Saved for the backward pass (4 bytes per position).
+ *   loss_rows  [T] float32 device, optional (NULL to skip): L_t per position.
+ */
+KD_API int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const float* logp,
+                    int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                    float* loss, float* lse, float* loss_rows,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* Backward. Recomputes each chunk's logits, forms dz (bf16, in ws), then
+ *   dH [T, d] float32 device, overwritten: dz W.
+ *   dW [V, d] float32 device: dz^T H. It is added to the existing contents
+ *      when accumulate_dW != 0, and overwritten otherwise.
+ *   lse        [T] float32 from kd_fused_kl_fwd on the same inputs.
+ *   grad_scale host float s, and grad_scale_dev an optional device float32
+ *              (NULL = 1) that multiplies s. The autograd binding passes
+ *              1/T here and the upstream gradient through grad_scale_dev, so
+ *              it never synchronises.
+ */
+KD_API int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const float* logp,
+                    const float* lse, int64_t T, int64_t d, int64_t V, int32_t K,
+                    int64_t chunk, float grad_scale, const float* grad_scale_dev,
+                    float* dH, float* dW, int32_t accumulate_dW,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns the status word kept in `ws` (KD_OK when no
+ * device-side error was recorded) and clears it. Returns KD_ERR_CUDA if the
+ * stream itself failed. */
+KD_API int kd_read_device_status(void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KD_H_ */

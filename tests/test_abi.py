@@ -1,0 +1,119 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+symbol the headers declare, and rejects bad arguments before any CUDA call.
+No GPU is needed."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from top_kl_loss_tcgen05_b300 import _native, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for h in ("kd.h", "kd_testing.h", "kd_profile.h"):
+        with open(os.path.join(ROOT, "include", h)) as f:
+            src = f.read()
+        names.update(re.findall(r"KD_API[^;(]*?\b(kd_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _native.load()
+
+
+def test_headers_declare_the_three_calls():
+    names = _declared_symbols()
+    for n in ("kd_topk_cache", "kd_fused_kl_fwd", "kd_fused_kl_bwd", "kd_fused_kl_workspace_size",
+              "kd_topk_workspace_size", "kd_read_device_status", "kd_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_symbols()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _native.SIGNATURES, n
+    # and nothing else is bound by the Python side
+    assert set(_native.SIGNATURES) == names
+
+
+def test_built_for_sm103a():
+    assert "arch=compute_103a,code=sm_103a" in build.ARCH
+    assert os.path.exists(build.LIB)
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "KD_OK"), (1, "KD_ERR_INVALID_ARG"), (2, "KD_ERR_UNSUPPORTED"), (3, "KD_ERR_WORKSPACE"),
+                       (4, "KD_ERR_CUDA"), (5, "KD_ERR_DEVICE_TIMEOUT"), (6, "KD_ERR_BAD_ID")]:
+        assert lib.kd_status_string(code).decode() == name
+    assert lib.kd_status_string(99).decode() == "KD_ERR_UNKNOWN"
+    assert lib.kd_version() >= 100
+
+
+def test_fused_workspace_is_independent_of_T_and_linear_in_chunk(lib):
+    f = lib.kd_fused_kl_workspace_size
+    a = f(2880, 201088, 100, 2048)
+    b = f(2880, 201088, 100, 4096)
+    assert a > 0 and b > 0
+    # dominated by the bf16 dz chunk: chunk * V * 2 bytes
+    assert 2048 * 201088 * 2 < a < 1.05 * 2048 * 201088 * 2 + 64 * 2**20
+    assert 1.9 < b / a < 2.1
+    assert f(0, 10, 1, 1) == 0 and f(8, 0, 1, 1) == 0 and f(8, 10, 0, 1) == 0 and f(8, 10, 1, 0) == 0
+
+
+# Fake but non-null "device" pointers: every call below must fail in argument
+# validation, before anything touches CUDA.
+P = ctypes.c_void_p(0x1000)
+P16 = ctypes.c_void_p(0x10000)
+
+
+def test_topk_argument_errors(lib):
+    ws = ctypes.c_void_p(0x100000)
+    call = lib.kd_topk_cache
+    assert call(None, 0, 4, 8, 8, 2, P16, P16, ws, 256, None) == _native.KD_ERR_INVALID_ARG
+    assert call(P16, 0, 0, 8, 8, 2, P16, P16, ws, 256, None) == _native.KD_ERR_INVALID_ARG
+    assert call(P16, 0, 4, 8, 8, 9, P16, P16, ws, 256, None) == _native.KD_ERR_INVALID_ARG  # K > V
+    assert call(P16, 0, 4, 8, 7, 2, P16, P16, ws, 256, None) == _native.KD_ERR_INVALID_ARG  # ld < V
+    assert call(P16, 7, 4, 8, 8, 2, P16, P16, ws, 256, None) == _native.KD_ERR_INVALID_ARG  # dtype
+    assert call(ctypes.c_void_p(0x1001), 0, 4, 8, 8, 2, P16, P16, ws, 256, None) == _native.KD_ERR_UNSUPPORTED
+    assert call(ctypes.c_void_p(0x1002), 1, 4, 8, 8, 2, P16, P16, ws, 256, None) == _native.KD_ERR_UNSUPPORTED
+    assert call(P16, 0, 4, 8, 8, 2, P16, P16, None, 256, None) == _native.KD_ERR_WORKSPACE
+    assert call(P16, 0, 4, 8, 8, 2, P16, P16, ws, 16, None) == _native.KD_ERR_WORKSPACE
+    assert call(P16, 0, 4, 8, 8, 2, P16, P16, ctypes.c_void_p(0x100010), 256, None) == _native.KD_ERR_WORKSPACE
+
+
+def test_fused_argument_errors(lib):
+    ws = ctypes.c_void_p(0x100000)
+    big = 1 << 40
+    fwd = lib.kd_fused_kl_fwd
+    args = dict(H=P16, W=P16, ids=P16, logp=P16, T=64, d=64, V=128, K=4, chunk=32, loss=P16, lse=P16, rows=None,
+                ws=ws, wsb=big, s=None)
+
+    def f(**kw):
+        a = dict(args)
+        a.update(kw)
+        return fwd(*a.values())
+
+    assert f(H=None) == _native.KD_ERR_INVALID_ARG
+    assert f(T=0) == _native.KD_ERR_INVALID_ARG
+    assert f(K=129) == _native.KD_ERR_INVALID_ARG
+    assert f(loss=None) == _native.KD_ERR_INVALID_ARG
+    assert f(d=60) == _native.KD_ERR_UNSUPPORTED  # d % 8
+    assert f(K=4097, V=5000) == _native.KD_ERR_UNSUPPORTED
+    assert f(W=ctypes.c_void_p(0x10008)) == _native.KD_ERR_UNSUPPORTED
+    assert f(wsb=10) == _native.KD_ERR_WORKSPACE
+    assert f(ws=None) == _native.KD_ERR_WORKSPACE
+    bwd = lib.kd_fused_kl_bwd
+    assert bwd(P16, P16, P16, P16, None, 64, 64, 128, 4, 32, 1.0, None, P16, P16, 0, ws, big, None) == \
+        _native.KD_ERR_INVALID_ARG
+    assert bwd(P16, P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, None, P16, 0, ws, big, None) == \
+        _native.KD_ERR_INVALID_ARG
+    assert bwd(P16, P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, ctypes.c_void_p(0x10004), P16, 0, ws,
+               big, None) == _native.KD_ERR_UNSUPPORTED

@@ -1,0 +1,55 @@
+"""The tcgen05 GEMM building block (TMA -> smem -> tcgen05.mma -> TMEM -> TMA
+store / reduce-add) against a plain PyTorch fp64 product of the same bf16
+operands, for every operand layout the backward pass uses and ragged edges in
+M, N and K."""
+
+import pytest
+import torch
+
+from top_kl_loss_tcgen05_b300 import _native, workspace
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(M, N, K, a_mn, b_mn, reduce_add=False, seed=0):
+    dev = torch.device("cuda:0")
+    g = torch.Generator(device=dev).manual_seed(seed)
+    A = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g, device=dev).to(torch.bfloat16)
+    Ain = A.t().contiguous() if a_mn else A.contiguous()
+    Bin = B.t().contiguous() if b_mn else B.contiguous()
+    C0 = torch.randn(M, N, generator=g, device=dev) if reduce_add else torch.full((M, N), float("nan"), device=dev)
+    C = C0.clone()
+    ws = workspace(256, dev)
+    rc = _native.lib().kd_test_gemm(Ain.data_ptr(), Bin.data_ptr(), C.data_ptr(), M, N, K, a_mn, b_mn,
+                                    1 if reduce_add else 0, ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, _native.status_string(rc)
+    assert _native.lib().kd_read_device_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+    ref = A.double() @ B.double().t()
+    if reduce_add:
+        ref = ref + C0.double()
+    err = (C.double() - ref).norm() / ref.norm()
+    assert torch.isfinite(C).all()
+    assert err < 1e-5, err.item()
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
+def test_gemm_layouts_exact_tiles(cuda_dev, a_mn, b_mn):
+    _run(256, 384, 256, a_mn, b_mn)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
+def test_gemm_layouts_ragged(cuda_dev, a_mn, b_mn):
+    _run(136, 200, 72, a_mn, b_mn, seed=1)
+    _run(1000, 584, 1032, a_mn, b_mn, seed=2)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 1), (1, 1)])
+def test_gemm_reduce_add(cuda_dev, a_mn, b_mn):
+    _run(520, 392, 200, a_mn, b_mn, reduce_add=True, seed=3)
+
+
+def test_gemm_many_tiles_persistent(cuda_dev):
+    # more tiles than SMs: every CTA loops over several tiles and both TMEM
+    # accumulators
+    _run(128 * 40, 192 * 9, 128, 0, 1, seed=4)

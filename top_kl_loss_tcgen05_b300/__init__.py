@@ -1,0 +1,193 @@
+"""Offline top-K knowledge distillation on one B300 (sm_103a).
+
+Python side of libkd (C ABI in include/kd.h). PyTorch supplies device memory
+and the current stream. Every step of the computation runs in libkd's CUDA
+kernels. This module only checks shapes and passes pointers.
+
+    ids, logp = topk_cache(teacher_logits, K)                  # offline cache
+    loss = FusedKL.apply(H, W, ids, logp, chunk)               # fused chunked KL
+    loss.backward()                                            # dH, dW
+
+The method: "ทำให้ Knowledge Distillation มีประสิทธิภาพ คุ้มค่า และใช้งานได้จริงใน
+ระดับ Scale ใหญ่" (ai-thai.com), sections "การทำ Distillation แบบ Offline" (the
+top-K cache) and "กลไก Fused Chunked KL Loss" (the fused chunked loss).
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import _native
+from ._native import KDError, check, status_string  # noqa: F401
+
+__all__ = [
+    "topk_cache",
+    "fused_kl_workspace",
+    "fused_kl_fwd",
+    "fused_kl_bwd",
+    "FusedKL",
+    "read_device_status",
+    "KDError",
+]
+
+_WS_ALIGN = 256
+
+
+def _stream_ptr(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A caller-owned workspace (uint8, 256-byte aligned) of at least nbytes."""
+    buf = torch.empty(int(nbytes) + _WS_ALIGN, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % _WS_ALIGN
+    ws = buf[off : off + int(nbytes)]
+    ws.zero_()
+    return ws
+
+
+def read_device_status(ws: torch.Tensor) -> int:
+    """Synchronise the current stream; return and clear the workspace status word."""
+    return _native.lib().kd_read_device_status(ws.data_ptr(), _stream_ptr(ws.device))
+
+
+# ----------------------------------------------------------------- top-K cache
+
+
+def topk_cache(logits: torch.Tensor, K: int, ws: torch.Tensor | None = None):
+    """Teacher logits [T, V] (bf16 or fp32, rows may be strided) ->
+    (ids int32 [T, K], logp float32 [T, K]): the K largest logits per row,
+    value-descending then id-ascending, and their full-vocabulary log-softmax."""
+    if logits.dim() != 2:
+        raise ValueError("logits must be [T, V]")
+    if logits.dtype == torch.bfloat16:
+        dt = _native.KD_BF16
+    elif logits.dtype == torch.float32:
+        dt = _native.KD_F32
+    else:
+        raise TypeError("logits must be bf16 or fp32")
+    if not logits.is_cuda or logits.stride(1) != 1:
+        raise ValueError("logits must be a CUDA tensor with unit column stride")
+    T, V = logits.shape
+    dev = logits.device
+    ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+    logp = torch.empty(T, K, dtype=torch.float32, device=dev)
+    L = _native.lib()
+    need = L.kd_topk_workspace_size(T, V, K, dt)
+    if ws is None:
+        ws = workspace(need, dev)
+    check(
+        "kd_topk_cache",
+        L.kd_topk_cache(logits.data_ptr(), dt, T, V, logits.stride(0), K, ids.data_ptr(), logp.data_ptr(),
+                        ws.data_ptr(), ws.numel(), _stream_ptr(dev)),
+    )
+    return ids, logp
+
+
+# ----------------------------------------------------------------- fused KL
+
+
+def fused_kl_workspace(d: int, V: int, K: int, chunk: int, device) -> torch.Tensor:
+    n = _native.lib().kd_fused_kl_workspace_size(d, V, K, chunk)
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return workspace(n, device)
+
+
+def _check_fused(H, W, ids, logp):
+    _need(H, "H", torch.bfloat16)
+    dev = H.device
+    _need(W, "W", torch.bfloat16, dev)
+    _need(ids, "ids", torch.int32, dev)
+    _need(logp, "logp", torch.float32, dev)
+    if H.dim() != 2 or W.dim() != 2 or H.shape[1] != W.shape[1]:
+        raise ValueError("H [T, d] and W [V, d] required")
+    if ids.shape != logp.shape or ids.dim() != 2 or ids.shape[0] != H.shape[0]:
+        raise ValueError("ids and logp must be [T, K]")
+    return H.shape[0], H.shape[1], W.shape[0], ids.shape[1]
+
+
+def fused_kl_fwd(H, W, ids, logp, chunk: int, ws=None, want_rows: bool = False):
+    """Forward: (loss [] f32, lse [T] f32, loss_rows [T] f32 or None)."""
+    T, d, V, K = _check_fused(H, W, ids, logp)
+    dev = H.device
+    if ws is None:
+        ws = fused_kl_workspace(d, V, K, chunk, dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    rows = torch.empty(T, dtype=torch.float32, device=dev) if want_rows else None
+    check(
+        "kd_fused_kl_fwd",
+        _native.lib().kd_fused_kl_fwd(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K,
+                                      chunk, loss.data_ptr(), lse.data_ptr(), _ptr(rows), ws.data_ptr(),
+                                      ws.numel(), _stream_ptr(dev)),
+    )
+    return loss, lse, rows
+
+
+def fused_kl_bwd(H, W, ids, logp, lse, chunk: int, grad_scale: float, grad_scale_dev=None, dH=None, dW=None,
+                 accumulate_dW: bool = False, ws=None):
+    """Backward: (dH [T, d] f32, dW [V, d] f32) for dz = s (q - p)."""
+    T, d, V, K = _check_fused(H, W, ids, logp)
+    dev = H.device
+    _need(lse, "lse", torch.float32, dev)
+    if ws is None:
+        ws = fused_kl_workspace(d, V, K, chunk, dev)
+    if dH is None:
+        dH = torch.empty(T, d, dtype=torch.float32, device=dev)
+    if dW is None:
+        dW = torch.empty(V, d, dtype=torch.float32, device=dev)
+    _need(dH, "dH", torch.float32, dev)
+    _need(dW, "dW", torch.float32, dev)
+    if grad_scale_dev is not None:
+        _need(grad_scale_dev, "grad_scale_dev", torch.float32, dev)
+    check(
+        "kd_fused_kl_bwd",
+        _native.lib().kd_fused_kl_bwd(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), lse.data_ptr(),
+                                      T, d, V, K, chunk, float(grad_scale), _ptr(grad_scale_dev), dH.data_ptr(),
+                                      dW.data_ptr(), 1 if accumulate_dW else 0, ws.data_ptr(), ws.numel(),
+                                      _stream_ptr(dev)),
+    )
+    return dH, dW
+
+
+class FusedKL(torch.autograd.Function):
+    """loss = mean_t KL(p_teacher,topK || softmax(W h_t)), fused and chunked.
+
+    Forward saves only lse [T] (4 bytes per position). Backward recomputes
+    each chunk's logits. The upstream gradient goes to the kernels as a
+    device scalar, so backward does not synchronise.
+    """
+
+    @staticmethod
+    def forward(ctx, H, W, ids, logp, chunk: int):
+        ws = fused_kl_workspace(H.shape[1], W.shape[0], ids.shape[1], chunk, H.device)
+        loss, lse, _ = fused_kl_fwd(H, W, ids, logp, chunk, ws=ws)
+        ctx.save_for_backward(H, W, ids, logp, lse)
+        ctx.chunk = chunk
+        ctx.ws = ws
+        return loss
+
+    @staticmethod
+    def backward(ctx, g):
+        H, W, ids, logp, lse = ctx.saved_tensors
+        g = g.detach().to(torch.float32).contiguous()
+        dH, dW = fused_kl_bwd(H, W, ids, logp, lse, ctx.chunk, 1.0 / H.shape[0], grad_scale_dev=g, ws=ctx.ws)
+        return dH.to(H.dtype), dW.to(W.dtype), None, None, None

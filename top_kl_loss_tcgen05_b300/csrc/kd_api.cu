@@ -1,0 +1,489 @@
+// kd_api.cu - the C ABI of libkd: argument checks, workspace layout, the
+// chunk loop of the fused KL loss, and the launches.
+//
+// The chunk loop is the structure of the "Fused chunked KL" variant ("ทำให้
+// Knowledge Distillation มีประสิทธิภาพ..." (ai-thai.com), section "กลไก Fused
+// Chunked KL Loss"; "Multiverse Computing сократила видеопамять..."
+// (iitog.ru), fourth paragraph). Positions are processed one chunk at a time:
+//   forward : prep -> logits GEMM with (max, sum, gather) epilogue -> merge
+//   backward: prep -> logits GEMM recompute with dz epilogue -> dH + dW GEMMs
+// The only per-chunk buffers (in the caller's workspace) are O(chunk * V):
+// the bf16 dz of one chunk and the per-tile partials. Nothing grows with T
+// apart from the caller's own inputs and outputs.
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "../../include/kd.h"
+#include "../../include/kd_profile.h"
+#include "../../include/kd_testing.h"
+#include "kd_internal.h"
+
+namespace kd {
+
+namespace {
+
+constexpr size_t kHeader = 256;  // status word, counters, fp64 loss accumulator
+constexpr size_t kAccOffset = 128;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode() {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+int num_sms_current() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Fused-loss workspace layout (all offsets 256-byte aligned; dz 1024).
+struct Layout {
+  int Kp;
+  int64_t S;    // vocabulary tiles of the forward GEMM
+  int64_t ldz;  // dz row stride in elements
+  size_t ids_sorted, p_sorted, cnt, ent, zK, block_sums, part_m, part_s, dz, total;
+};
+
+Layout fused_layout(int64_t d, int64_t V, int K, int64_t chunk) {
+  (void)d;
+  Layout L;
+  L.Kp = (K + 3) / 4 * 4;
+  L.S = ceil_div(V, kBNLogits);
+  L.ldz = align_up((size_t)V, 64);
+  size_t o = kHeader;
+  auto take = [&](size_t bytes, size_t al) {
+    o = align_up(o, al);
+    const size_t r = o;
+    o += bytes;
+    return r;
+  };
+  L.ids_sorted = take((size_t)chunk * L.Kp * 4, 256);
+  L.p_sorted = take((size_t)chunk * L.Kp * 4, 256);
+  L.cnt = take((size_t)chunk * 4, 256);
+  L.ent = take((size_t)chunk * 4, 256);
+  L.zK = take((size_t)chunk * L.Kp * 4, 256);
+  L.block_sums = take((size_t)ceil_div(chunk, 32) * 8, 256);
+  L.part_m = take((size_t)L.S * chunk * 4, 256);
+  L.part_s = take((size_t)L.S * chunk * 4, 256);
+  L.dz = take((size_t)chunk * L.ldz * 2, 1024);
+  L.total = align_up(o, 256);
+  return L;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------------ profiling
+// Kernel names reported by kd_profile_end, indexed by KernelId.
+enum KernelId { K_TOPK, K_PREP, K_LOGITS_FWD, K_MERGE, K_REDUCE, K_FINALIZE, K_LOGITS_DZ, K_GRAD, K_TEST, K_COUNT };
+const char* const kKernelNames[K_COUNT] = {"topk_cache", "teacher_prep", "logits_fwd_lse_gather", "lse_merge_loss",
+                                           "loss_chunk_reduce", "loss_finalize", "logits_dz", "grad_dH_dW",
+                                           "test_gemm"};
+struct ProfRec {
+  int kid;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Records an event before the launch (constructor) and after it (destructor)
+// on the launch stream, while profiling is on.
+struct ProfScope {
+  int kid;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  ProfScope(int k, cudaStream_t st) : kid(k), s(st) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    if (!g_prof_on) return;
+    a = prof_event();
+    if (a && cudaEventRecord(a, s) != cudaSuccess) a = nullptr;
+  }
+  ~ProfScope() {
+    if (!a) return;
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    cudaEvent_t b = prof_event();
+    if (b && cudaEventRecord(b, s) == cudaSuccess) g_prof_recs.push_back({kid, a, b});
+  }
+};
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return KD_OK;
+  if (std::getenv("KD_DEBUG")) std::fprintf(stderr, "libkd: CUDA error %s\n", cudaGetErrorString(e));
+  return KD_ERR_CUDA;
+}
+
+int check_fused_args(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
+                     int64_t V, int32_t K, int64_t chunk, void* ws, size_t ws_bytes) {
+  if (!H || !W || !ids || !logp || T <= 0 || d <= 0 || V <= 0 || K <= 0 || chunk <= 0) return KD_ERR_INVALID_ARG;
+  if (K > V) return KD_ERR_INVALID_ARG;
+  if (K > 4096 || V >= (int64_t(1) << 31) || d % 8 != 0 || d > (int64_t(1) << 24) || chunk > (int64_t(1) << 24))
+    return KD_ERR_UNSUPPORTED;
+  if (!aligned(H, 16) || !aligned(W, 16)) return KD_ERR_UNSUPPORTED;
+  const Layout L = fused_layout(d, V, K, chunk);
+  if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return KD_ERR_WORKSPACE;
+  return KD_OK;
+}
+
+}  // namespace
+
+cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace kd
+
+using namespace kd;
+
+extern "C" {
+
+const char* kd_status_string(int status) {
+  switch (status) {
+    case KD_OK: return "KD_OK";
+    case KD_ERR_INVALID_ARG: return "KD_ERR_INVALID_ARG";
+    case KD_ERR_UNSUPPORTED: return "KD_ERR_UNSUPPORTED";
+    case KD_ERR_WORKSPACE: return "KD_ERR_WORKSPACE";
+    case KD_ERR_CUDA: return "KD_ERR_CUDA";
+    case KD_ERR_DEVICE_TIMEOUT: return "KD_ERR_DEVICE_TIMEOUT";
+    case KD_ERR_BAD_ID: return "KD_ERR_BAD_ID";
+    default: return "KD_ERR_UNKNOWN";
+  }
+}
+
+int kd_version(void) { return 100; }
+
+size_t kd_topk_workspace_size(int64_t T, int64_t V, int32_t K, int32_t dtype) {
+  (void)T; (void)V; (void)K; (void)dtype;
+  return kHeader;
+}
+
+int kd_topk_cache(const void* logits, int32_t dtype, int64_t T, int64_t V, int64_t ld, int32_t K, int32_t* ids,
+                  float* logp, void* ws, size_t ws_bytes, void* stream) {
+  if (!logits || !ids || !logp || T <= 0 || V <= 0 || K <= 0 || K > V || ld < V) return KD_ERR_INVALID_ARG;
+  if (dtype != KD_BF16 && dtype != KD_F32) return KD_ERR_INVALID_ARG;
+  if (V >= (int64_t(1) << 31) || K > 65536) return KD_ERR_UNSUPPORTED;
+  if (!aligned(logits, dtype == KD_BF16 ? 2 : 4)) return KD_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < kHeader) return KD_ERR_WORKSPACE;
+  if (topk_smem_bytes(K) > 200 * 1024) return KD_ERR_UNSUPPORTED;
+  const int sms = num_sms_current();
+  if (sms <= 0) return KD_ERR_CUDA;
+  const char* fe = std::getenv("KD_TOPK_FORCE_EXACT");
+  const int force = (fe && fe[0] == '1') ? 1 : 0;
+  ProfScope ps(K_TOPK, static_cast<cudaStream_t>(stream));
+  return cuda_status(launch_topk(logits, dtype, T, V, ld, K, ids, logp, static_cast<int*>(ws), force, sms,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+size_t kd_fused_kl_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk) {
+  if (d <= 0 || V <= 0 || K <= 0 || chunk <= 0) return 0;
+  return fused_layout(d, V, K, chunk).total;
+}
+
+int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
+                    int64_t V, int32_t K, int64_t chunk, float* loss, float* lse, float* loss_rows, void* ws,
+                    size_t ws_bytes, void* stream) {
+  int st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, ws, ws_bytes);
+  if (st != KD_OK) return st;
+  if (!loss || !lse) return KD_ERR_INVALID_ARG;
+  const int sms = num_sms_current();
+  if (sms <= 0) return KD_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = fused_layout(d, V, K, chunk);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* status = reinterpret_cast<int*>(w);
+  double* acc = reinterpret_cast<double*>(w + kAccOffset);
+  int* ids_sorted = reinterpret_cast<int*>(w + L.ids_sorted);
+  float* p_sorted = reinterpret_cast<float*>(w + L.p_sorted);
+  int* cnt = reinterpret_cast<int*>(w + L.cnt);
+  float* ent = reinterpret_cast<float*>(w + L.ent);
+  float* zK = reinterpret_cast<float*>(w + L.zK);
+  double* bsum = reinterpret_cast<double*>(w + L.block_sums);
+  float* part_m = reinterpret_cast<float*>(w + L.part_m);
+  float* part_s = reinterpret_cast<float*>(w + L.part_s);
+  const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
+
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  cudaError_t e = encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V,
+                                (uint64_t)d * 2, kBK, kBNLogits);
+  if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
+  for (int64_t c0 = 0; c0 < T; c0 += chunk) {
+    const int rows = (int)((T - c0) < chunk ? (T - c0) : chunk);
+    {
+      ProfScope ps(K_PREP, s);
+      e = launch_prep(ids + c0 * K, logp + c0 * K, rows, K, (int)V, L.Kp, ids_sorted, p_sorted, cnt, ent, status, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    e = encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + c0 * d, (uint64_t)d, (uint64_t)rows,
+                      (uint64_t)d * 2, kBK, kBM);
+    if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
+    Problem& P = a.pr[0];
+    P.m_blocks = (int)ceil_div(rows, kBM);
+    P.n_blocks = (int)ceil_div(V, kBNLogits);
+    P.k_blocks = (int)ceil_div(d, kBK);
+    P.a_mn = 0; P.b_mn = 0;
+    P.M = rows; P.N = (int)V;
+    P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0;
+    a.nprob = 1;
+    a.total_tiles = P.m_blocks * P.n_blocks;
+    a.rows = rows; a.row_stride = (int)chunk; a.V = (int)V; a.Kp = L.Kp;
+    a.ids_sorted = ids_sorted; a.p_sorted = p_sorted; a.cnt = cnt;
+    a.zK = zK; a.part_m = part_m; a.part_s = part_s;
+    a.status = status;
+    {
+      ProfScope ps(K_LOGITS_FWD, s);
+      e = launch_logits_fwd(a, sms, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    {
+      ProfScope ps(K_MERGE, s);
+      e = launch_merge(part_m, part_s, (int)L.S, rows, (int)chunk, ent, p_sorted, zK, cnt, L.Kp, lse + c0,
+                       loss_rows ? loss_rows + c0 : nullptr, bsum, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    {
+      ProfScope ps(K_REDUCE, s);
+      e = launch_chunk_reduce(bsum, (int)ceil_div(rows, 32), acc, c0 == 0, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  ProfScope ps(K_FINALIZE, s);
+  return cuda_status(launch_finalize(acc, 1.0 / (double)T, loss, s));
+}
+
+int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const float* logp, const float* lse,
+                    int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk, float grad_scale,
+                    const float* grad_scale_dev, float* dH, float* dW, int32_t accumulate_dW, void* ws,
+                    size_t ws_bytes, void* stream) {
+  int st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, ws, ws_bytes);
+  if (st != KD_OK) return st;
+  if (!lse || !dH || !dW) return KD_ERR_INVALID_ARG;
+  if (!aligned(dH, 16) || !aligned(dW, 16)) return KD_ERR_UNSUPPORTED;
+  const int sms = num_sms_current();
+  if (sms <= 0) return KD_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = fused_layout(d, V, K, chunk);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* status = reinterpret_cast<int*>(w);
+  int* ids_sorted = reinterpret_cast<int*>(w + L.ids_sorted);
+  float* p_sorted = reinterpret_cast<float*>(w + L.p_sorted);
+  int* cnt = reinterpret_cast<int*>(w + L.cnt);
+  float* ent = reinterpret_cast<float*>(w + L.ent);
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(w + L.dz);
+  const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
+
+  GemmArgs az, ag;
+  std::memset(&az, 0, sizeof(az));
+  std::memset(&ag, 0, sizeof(ag));
+  cudaError_t e;
+  // W as the K-major B of the logits GEMM and the N-major B of dH.
+  e = encode_map_2d(&az.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2,
+                    kBK, kBNLogits);
+  if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
+  e = encode_map_2d(&ag.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, 64,
+                    64);
+  if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
+  e = encode_map_2d(&ag.tmC[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, (uint64_t)d, (uint64_t)V, (uint64_t)d * 4, 32,
+                    32);
+  if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
+
+  for (int64_t c0 = 0; c0 < T; c0 += chunk) {
+    const int rows = (int)((T - c0) < chunk ? (T - c0) : chunk);
+    {
+      ProfScope ps(K_PREP, s);
+      e = launch_prep(ids + c0 * K, logp + c0 * K, rows, K, (int)V, L.Kp, ids_sorted, p_sorted, cnt, ent, status, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+
+    // Recompute the chunk's logits; the epilogue writes dz (bf16).
+    if (encode_map_2d(&az.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + c0 * d, (uint64_t)d, (uint64_t)rows,
+                      (uint64_t)d * 2, kBK, kBM) != cudaSuccess ||
+        encode_map_2d(&az.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)rows,
+                      (uint64_t)L.ldz * 2, 64, 32) != cudaSuccess)
+      return KD_ERR_UNSUPPORTED;
+    {
+      Problem& P = az.pr[0];
+      P.m_blocks = (int)ceil_div(rows, kBM);
+      P.n_blocks = (int)ceil_div(V, kBNLogits);
+      P.k_blocks = (int)ceil_div(d, kBK);
+      P.a_mn = 0; P.b_mn = 0; P.M = rows; P.N = (int)V;
+      P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0;
+      az.nprob = 1;
+      az.total_tiles = P.m_blocks * P.n_blocks;
+      az.rows = rows; az.row_stride = (int)chunk; az.V = (int)V; az.Kp = L.Kp;
+      az.ids_sorted = ids_sorted; az.p_sorted = p_sorted; az.cnt = cnt;
+      az.lse = lse + c0; az.scale = grad_scale; az.dscale = grad_scale_dev;
+      az.status = status;
+    }
+    {
+      ProfScope ps(K_LOGITS_DZ, s);
+      e = launch_logits_dz(az, sms, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+
+    // dH_c = dz W (problem 0) and dW (+)= dz^T H_c (problem 1), one launch.
+    if (encode_map_2d(&ag.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)rows,
+                      (uint64_t)L.ldz * 2, kBK, kBM) != cudaSuccess ||
+        encode_map_2d(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dH + c0 * d, (uint64_t)d, (uint64_t)rows,
+                      (uint64_t)d * 4, 32, 32) != cudaSuccess ||
+        encode_map_2d(&ag.tmA[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)rows,
+                      (uint64_t)L.ldz * 2, 64, 64) != cudaSuccess ||
+        encode_map_2d(&ag.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + c0 * d, (uint64_t)d, (uint64_t)rows,
+                      (uint64_t)d * 2, 64, 64) != cudaSuccess)
+      return KD_ERR_UNSUPPORTED;
+    {
+      Problem& P0 = ag.pr[0];
+      P0.m_blocks = (int)ceil_div(rows, kBM);
+      P0.n_blocks = (int)ceil_div(d, kBNGrad);
+      P0.k_blocks = (int)ceil_div(V, kBK);
+      P0.a_mn = 0; P0.b_mn = 1; P0.M = rows; P0.N = (int)d;
+      P0.tile_begin = 0; P0.n_fastest = 0; P0.reduce_add = 0;
+      Problem& P1 = ag.pr[1];
+      P1.m_blocks = (int)ceil_div(V, kBM);
+      P1.n_blocks = (int)ceil_div(d, kBNGrad);
+      P1.k_blocks = (int)ceil_div(rows, kBK);
+      P1.a_mn = 1; P1.b_mn = 1; P1.M = (int)V; P1.N = (int)d;
+      P1.tile_begin = P0.m_blocks * P0.n_blocks; P1.n_fastest = 1;
+      P1.reduce_add = (accumulate_dW || c0 > 0) ? 1 : 0;
+      ag.nprob = 2;
+      ag.total_tiles = P1.tile_begin + P1.m_blocks * P1.n_blocks;
+      ag.status = status;
+    }
+    {
+      ProfScope ps(K_GRAD, s);
+      e = launch_grad(ag, sms, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return KD_OK;
+}
+
+int kd_read_device_status(void* ws, void* stream) {
+  if (!ws) return KD_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KD_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KD_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return KD_ERR_CUDA;
+  return v;
+}
+
+int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int32_t a_mn,
+                 int32_t b_mn, int32_t reduce_add, void* ws, void* stream) {
+  if (!A || !B || !C || !ws || M <= 0 || N <= 0 || K <= 0) return KD_ERR_INVALID_ARG;
+  if (K % 8 || (a_mn && M % 8) || (b_mn && N % 8) || N % 4) return KD_ERR_UNSUPPORTED;
+  if (M >= (1 << 30) || N >= (1 << 30) || K >= (1 << 30)) return KD_ERR_UNSUPPORTED;
+  const int sms = num_sms_current();
+  if (sms <= 0) return KD_ERR_CUDA;
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  cudaError_t e1 = a_mn ? encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, M, K, M * 2, 64, 64)
+                        : encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, kBK, kBM);
+  cudaError_t e2 = b_mn ? encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, N * 2, 64, 64)
+                        : encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, K * 2, kBK, kBNGrad);
+  cudaError_t e3 = encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, 32);
+  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return KD_ERR_UNSUPPORTED;
+  Problem& P = a.pr[0];
+  P.m_blocks = (int)ceil_div(M, kBM);
+  P.n_blocks = (int)ceil_div(N, kBNGrad);
+  P.k_blocks = (int)ceil_div(K, kBK);
+  P.a_mn = a_mn ? 1 : 0; P.b_mn = b_mn ? 1 : 0;
+  P.M = (int)M; P.N = (int)N;
+  P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = reduce_add ? 1 : 0;
+  a.nprob = 1;
+  a.total_tiles = P.m_blocks * P.n_blocks;
+  a.status = static_cast<int*>(ws);
+  ProfScope ps(K_TEST, static_cast<cudaStream_t>(stream));
+  return cuda_status(launch_grad(a, sms, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+extern "C" {
+
+int kd_profile_begin(void) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  for (auto& r : g_prof_recs) {
+    g_prof_pool.push_back(r.a);
+    g_prof_pool.push_back(r.b);
+  }
+  g_prof_recs.clear();
+  g_prof_on = true;
+  return KD_OK;
+}
+
+int kd_profile_end(kd_prof_entry* out, int32_t max_entries, int32_t* n_out) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  g_prof_on = false;
+  int launches[K_COUNT] = {0};
+  double ms[K_COUNT] = {0.0};
+  int rc = KD_OK;
+  for (auto& r : g_prof_recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) {
+      rc = KD_ERR_CUDA;
+    } else {
+      launches[r.kid] += 1;
+      ms[r.kid] += t;
+    }
+    g_prof_pool.push_back(r.a);
+    g_prof_pool.push_back(r.b);
+  }
+  g_prof_recs.clear();
+  int n = 0;
+  for (int k = 0; k < K_COUNT; ++k) {
+    if (!launches[k]) continue;
+    if (out && n < max_entries) {
+      std::memset(out[n].name, 0, sizeof(out[n].name));
+      std::strncpy(out[n].name, kKernelNames[k], sizeof(out[n].name) - 1);
+      out[n].launches = launches[k];
+      out[n].total_ms = ms[k];
+      ++n;
+    }
+  }
+  if (n_out) *n_out = n;
+  return rc;
+}
+
+}  // extern "C"

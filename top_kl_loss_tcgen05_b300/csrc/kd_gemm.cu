@@ -1,0 +1,441 @@
+// kd_gemm.cu - the projection GEMMs of the fused chunked KL loss on tcgen05.
+//
+// The three GEMM shapes of the method ("ทำให้ Knowledge Distillation มี
+// ประสิทธิภาพ..." (ai-thai.com), section "กลไก Fused Chunked KL Loss": hidden
+// states -> logits per chunk, loss accumulated, chunk discarded; backward
+// recomputes each chunk):
+//   logits  z = H_c W^T    A = H_c [c, d] K-major, B = W [V, d] K-major
+//   dH      dz W           A = dz [c, V] K-major,  B = W [V, d] N-major
+//   dW      dz^T H_c       A = dz [c, V] M-major,  B = H_c [c, d] N-major
+// All run in one persistent, warp-specialised kernel template:
+//   warp 0     TMA producer: one thread streams A/B tiles into a ring of
+//              shared-memory stages (128-byte swizzle).
+//   warp 1     MMA issuer: one thread issues tcgen05.mma (M=128, N=BN,
+//              K=16) into one of two TMEM accumulators. tcgen05.commit frees
+//              the smem stage, and then signals the finished accumulator.
+//   warps 2-5  epilogue: tcgen05.ld the accumulator (each warp owns 32 TMEM
+//              lanes = 32 rows). While the MMA warp fills the other
+//              accumulator, they run the fused math:
+//     EPI_FWD   online (max, sum exp) per row over the tile's vocabulary
+//               slice, and the logits at the teacher ids that fall in it;
+//     EPI_DZ    dz = s (exp(z - lse) - p [j in K]) -> bf16 -> TMA store;
+//     EPI_GRAD  fp32 tile -> TMA store (dH) or TMA reduce-add (dW += ...).
+// The logits tile therefore never leaves the chip in the forward pass. In
+// backward, only the chunk's dz (bf16, c x V) goes to HBM.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kd_internal.h"
+#include "kd_ptx.cuh"
+
+namespace kd {
+namespace {
+
+constexpr int EPI_FWD = 0, EPI_DZ = 1, EPI_GRAD = 2;
+constexpr int kThreads = 192;  // 6 warps
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kStageBytesStaging = 4096;  // one 32-row x 128-byte staging buffer
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kNone = 0xFFFFFFFFu;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int BN, int NS, int EPI>
+struct Cfg {
+  static constexpr uint32_t A_BYTES = kBM * kBK * 2;
+  static constexpr uint32_t B_BYTES = BN * kBK * 2;
+  static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
+  static constexpr uint32_t STG = (EPI == EPI_FWD) ? 0u : 4u * 2u * kStageBytesStaging;
+  static constexpr uint32_t BAR_OFF = NS * STAGE + STG;
+  static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+};
+
+struct Tile {
+  int prob, mb, nb;
+};
+
+__device__ __forceinline__ Tile decode(const GemmArgs& g, int t) {
+  Tile r;
+  r.prob = (g.nprob > 1 && t >= g.pr[1].tile_begin) ? 1 : 0;
+  const Problem& P = g.pr[r.prob];
+  const int i = t - P.tile_begin;
+  if (P.n_fastest) {
+    r.nb = i % P.n_blocks;
+    r.mb = i / P.n_blocks;
+  } else {
+    r.mb = i % P.m_blocks;
+    r.nb = i / P.m_blocks;
+  }
+  return r;
+}
+
+// First index k in the ascending list rid[0..cnt) with rid[k] >= x.
+__device__ __forceinline__ int lower_bound(const int* rid, int cnt, int x) {
+  int lo = 0, hi = cnt;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(rid + mid) < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+template <int BN, int NS, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs g) {
+  using C = Cfg<BN, NS, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* full = bars;              // [NS] TMA -> MMA
+  uint64_t* empty = bars + NS;        // [NS] MMA -> TMA
+  uint64_t* tfull = bars + 2 * NS;    // [2]  MMA -> epilogue
+  uint64_t* tempty = bars + 2 * NS + 2;  // [2] epilogue -> MMA
+  uint64_t* drain = bars + 2 * NS + 4;   // MMA drain on abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NS + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int p = 0; p < g.nprob; ++p) {
+      tma_prefetch_desc(&g.tmA[p]);
+      tma_prefetch_desc(&g.tmB[p]);
+      if (EPI != EPI_FWD) tma_prefetch_desc(&g.tmC[p]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, ipar = 0;  // per-stage bit: load issued / its phase parity
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < g.total_tiles; t += gridDim.x) {
+        const Tile tl = decode(g, t);
+        const Problem& P = g.pr[tl.prob];
+        const CUtensorMap* mA = &g.tmA[tl.prob];
+        const CUtensorMap* mB = &g.tmB[tl.prob];
+        for (int kb = 0; kb < P.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], C::STAGE);
+          const uint32_t sA = smem_u32(smem + stage * C::STAGE);
+          const uint32_t sB = sA + C::A_BYTES;
+          if (!P.a_mn) {
+            tma_load_2d(sA, mA, &full[stage], kb * kBK, tl.mb * kBM);
+          } else {
+#pragma unroll
+            for (int q = 0; q < kBM / 64; ++q) tma_load_2d(sA + q * 8192, mA, &full[stage], tl.mb * kBM + q * 64, kb * kBK);
+          }
+          if (!P.b_mn) {
+            tma_load_2d(sB, mB, &full[stage], kb * kBK, tl.nb * BN);
+          } else {
+#pragma unroll
+            for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * 8192, mB, &full[stage], tl.nb * BN + q * 64, kb * kBK);
+          }
+          issued |= 1u << stage;
+          ipar = (ipar & ~(1u << stage)) | (phase << stage);
+          if (++stage == NS) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        set_status(g.status, ST_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // Never leave the CTA while a TMA load may still write its smem: wait
+      // (bounded) until the last load issued into each stage has landed.
+      // Nothing else arrives on full[s] afterwards, so the phase it completes
+      // stays the most recent one and the parity wait returns. On the normal
+      // path every load was consumed already and this returns at once.
+      for (int st = 0; st < NS; ++st) {
+        if (!((issued >> st) & 1u)) continue;
+        const uint32_t a = smem_u32(&full[st]);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(a, (ipar >> st) & 1u)) {
+          if (globaltimer() - t0 > kWaitLimitNs) break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < g.total_tiles; t += gridDim.x) {
+        const Tile tl = decode(g, t);
+        const Problem& P = g.pr[tl.prob];
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const uint32_t idesc = idesc_bf16_f32(kBM, BN, P.a_mn, P.b_mn);
+        for (int kb = 0; kb < P.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(smem + stage * C::STAGE);
+          const uint32_t sB = sA + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = P.a_mn ? sdesc_sw128(sA + k * 2048, 8192, 1024) : sdesc_sw128(sA + k * 32, 16, 1024);
+            const uint64_t bd = P.b_mn ? sdesc_sw128(sB + k * 2048, 8192, 1024) : sdesc_sw128(sB + k * 32, 16, 1024);
+            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == NS) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok) {
+        set_status(g.status, ST_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // Let every MMA already issued finish before TMEM is released.
+      tc_commit(drain);
+      {
+        const uint32_t a = smem_u32(drain);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(a, 0u)) {
+          if (globaltimer() - t0 > kWaitLimitNs) break;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wq = warp & 3;  // TMEM lane quadrant this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int buf = 0, nstore = 0;
+    bool ok = true;
+    uint8_t* stg = smem + NS * C::STAGE + (uint32_t)wq * 2u * kStageBytesStaging;
+    for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
+      const Tile tl = decode(g, t);
+      const Problem& P = g.pr[tl.prob];
+      const int row_l = 32 * wq + lane;
+      const int row = tl.mb * kBM + row_l;
+      const int n0 = tl.nb * BN;
+
+      // Teacher-id cursor of this row for the tile's vocabulary slice.
+      int cnt = 0, k = 0;
+      const int* rid = nullptr;
+      int nvalid = 0;
+      if (EPI != EPI_GRAD) {
+        nvalid = min(BN, g.V - n0);
+        if (row < g.rows) {
+          cnt = __ldg(g.cnt + row);
+          rid = g.ids_sorted + (size_t)row * g.Kp;
+          k = lower_bound(rid, cnt, n0);
+        }
+      }
+
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) { ok = false; }
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(acc * BN);
+
+      if (EPI == EPI_FWD) {
+        float m = -INFINITY, s = 0.f;
+        for (int c0 = 0; c0 < nvalid; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c0, v);
+          tmem_wait_ld();
+          const int lim = nvalid - c0;
+          float cm = -INFINITY;
+          if (lim >= 32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cm = fmaxf(cm, u2f(v[j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) if (j < lim) cm = fmaxf(cm, u2f(v[j]));
+          }
+          const float mn = fmaxf(m, cm);
+          const float nb2 = -mn * kLog2e;
+          float acc_s = 0.f;
+          if (lim >= 32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc_s += ex2(fmaf(u2f(v[j]), kLog2e, nb2));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) if (j < lim) acc_s += ex2(fmaf(u2f(v[j]), kLog2e, nb2));
+          }
+          s = s * ex2((m - mn) * kLog2e) + acc_s;
+          m = mn;
+        }
+        // Logits at the teacher ids inside [n0, n0 + nvalid): one TMEM column
+        // per distinct id in the warp's 32 rows.
+        const uint32_t hiend = (uint32_t)(n0 + nvalid);
+        uint32_t want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
+        uint32_t u = __reduce_min_sync(0xffffffffu, want);
+        while (u != kNone) {
+          const uint32_t val = tmem_ld1(taddr + (u - (uint32_t)n0));
+          tmem_wait_ld();
+          if (want == u) {
+            g.zK[(size_t)row * g.Kp + k] = u2f(val);
+            ++k;
+            want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
+          }
+          u = __reduce_min_sync(0xffffffffu, want);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (row < g.rows) {
+          g.part_m[(size_t)tl.nb * g.row_stride + row] = m;
+          g.part_s[(size_t)tl.nb * g.row_stride + row] = s;
+        }
+      } else if (EPI == EPI_DZ) {
+        const float lse_r = (row < g.rows) ? __ldg(g.lse + row) : 0.f;
+        const float sc = g.scale * (g.dscale ? __ldg(g.dscale) : 1.f);
+        const float nl = -lse_r * kLog2e;
+        const bool box_live = tl.mb * kBM + 32 * wq < g.rows;
+        for (int c0 = 0; c0 < nvalid; c0 += 64) {
+          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
+          if (nstore >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c0 + 32 * h, v);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float e0 = ex2(fmaf(u2f(v[2 * j]), kLog2e, nl)) * sc;
+              const float e1 = ex2(fmaf(u2f(v[2 * j + 1]), kLog2e, nl)) * sc;
+              pk[j] = pack_bf16x2(e0, e1);
+            }
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const int q = h * 4 + qq;
+              st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4), pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2],
+                           pk[4 * qq + 3]);
+            }
+          }
+          // Teacher ids in this 64-column group: dz = s (q - p) in fp32.
+          const uint32_t hiend = (uint32_t)(n0 + min(c0 + 64, nvalid));
+          uint32_t want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
+          uint32_t u = __reduce_min_sync(0xffffffffu, want);
+          while (u != kNone) {
+            const uint32_t val = tmem_ld1(taddr + (u - (uint32_t)n0));
+            tmem_wait_ld();
+            if (want == u) {
+              const float q = ex2(fmaf(u2f(val), kLog2e, nl));
+              const float dz = sc * (q - __ldg(g.p_sorted + (size_t)row * g.Kp + k));
+              const int jj = (int)(u - (uint32_t)n0) - c0;
+              const __nv_bfloat16 hb = __float2bfloat16_rn(dz);
+              st_shared_u16(sb + lane * 128 + (((jj >> 3) ^ (lane & 7)) << 4) + ((jj & 7) << 1),
+                            *reinterpret_cast<const uint16_t*>(&hb));
+              ++k;
+              want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
+            }
+            u = __reduce_min_sync(0xffffffffu, want);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && box_live) {
+            tma_store_2d(&g.tmC[0], sb, n0 + c0, tl.mb * kBM + 32 * wq);
+          }
+          if (lane == 0) bulk_commit();
+          ++nstore;
+          buf ^= 1;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      } else {
+        const CUtensorMap* mC = &g.tmC[tl.prob];
+        const bool box_live = tl.mb * kBM + 32 * wq < P.M;
+        for (int c0 = 0; c0 < BN && n0 + c0 < P.N; c0 += 32) {
+          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
+          if (nstore >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+          uint32_t v[32];
+          tmem_ld32(taddr + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && box_live) {
+            if (P.reduce_add) tma_reduce_add_2d(mC, sb, n0 + c0, tl.mb * kBM + 32 * wq);
+            else tma_store_2d(mC, sb, n0 + c0, tl.mb * kBM + 32 * wq);
+          }
+          if (lane == 0) bulk_commit();
+          ++nstore;
+          buf ^= 1;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (!ok) {
+      if (lane == 0) { set_status(g.status, ST_TIMEOUT); *abort_flag = 1; }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int BN, int NS, int EPI>
+cudaError_t launch(const GemmArgs& a, int num_sms, cudaStream_t s) {
+  using C = Cfg<BN, NS, EPI>;
+  static_assert(C::SMEM <= 232448, "shared memory budget");
+  auto k = gemm_kernel<BN, NS, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  int grid = a.total_tiles < num_sms ? a.total_tiles : num_sms;
+  if (grid < 1) return cudaSuccess;
+  k<<<grid, kThreads, C::SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_logits_fwd(const GemmArgs& a, int num_sms, cudaStream_t s) {
+  return launch<kBNLogits, 4, EPI_FWD>(a, num_sms, s);
+}
+cudaError_t launch_logits_dz(const GemmArgs& a, int num_sms, cudaStream_t s) {
+  return launch<kBNLogits, 4, EPI_DZ>(a, num_sms, s);
+}
+cudaError_t launch_grad(const GemmArgs& a, int num_sms, cudaStream_t s) {
+  return launch<kBNGrad, 4, EPI_GRAD>(a, num_sms, s);
+}
+
+}  // namespace kd

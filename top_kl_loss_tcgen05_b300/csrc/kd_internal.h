@@ -1,0 +1,75 @@
+// kd_internal.h - host-side declarations shared by the libkd translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace kd {
+
+// Tile shape of the projection GEMMs: 128 rows of the M operand, BK = 64
+// reduction elements per pipeline stage (one 128-byte swizzle row of bf16).
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kBNLogits = 256;  // forward / recompute: N tile over the vocabulary
+constexpr int kBNGrad = 192;    // dH / dW: N tile over the hidden size d
+
+// One GEMM problem of a launch: C[M, N] = sum_k A[m, k] B[n, k].
+struct Problem {
+  int m_blocks, n_blocks, k_blocks;
+  int a_mn, b_mn;   // operand major-ness: 0 = K contiguous, 1 = M/N contiguous
+  int M, N;         // valid extents (epilogue stores are clipped to them)
+  int tile_begin;   // first global tile index of this problem
+  int n_fastest;    // tile order: 1 = consecutive tiles walk N, 0 = walk M
+  int reduce_add;   // fp32 epilogue: 1 = TMA reduce-add into C, 0 = store
+};
+
+// Kernel parameters (passed as __grid_constant__; tensor maps live in param space).
+struct GemmArgs {
+  CUtensorMap tmA[2];
+  CUtensorMap tmB[2];
+  CUtensorMap tmC[2];
+  Problem pr[2];
+  int nprob;
+  int total_tiles;
+  // fused-epilogue data (chunk-local rows)
+  int rows;               // rows of this chunk
+  int row_stride;         // stride of the [S][chunk] partial arrays (= chunk)
+  int V;
+  int Kp;                 // row stride of the sorted id / p / zK arrays
+  const int* ids_sorted;  // [chunk][Kp], ascending, padded
+  const float* p_sorted;  // [chunk][Kp]
+  const int* cnt;         // [chunk] entries per row
+  float* zK;              // [chunk][Kp] student logit at each sorted id
+  float* part_m;          // [S][chunk] per-(row, vocab tile) max
+  float* part_s;          // [S][chunk] per-(row, vocab tile) sum exp(z - max)
+  const float* lse;       // [rows] chunk slice of the saved log-sum-exp
+  float scale;            // dz scale
+  const float* dscale;    // optional device multiplier of `scale`
+  int* status;            // device status word
+};
+
+cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// Launchers (kd_gemm.cu).
+cudaError_t launch_logits_fwd(const GemmArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_logits_dz(const GemmArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_grad(const GemmArgs& a, int num_sms, cudaStream_t s);
+
+// Small kernels (kd_loss_aux.cu).
+cudaError_t launch_prep(const int32_t* ids, const float* logp, int rows, int K, int V, int Kp, int* ids_sorted,
+                        float* p_sorted, int* cnt, float* ent, int* status, cudaStream_t s);
+cudaError_t launch_merge(const float* part_m, const float* part_s, int S, int rows, int row_stride,
+                         const float* ent, const float* p_sorted, const float* zK, const int* cnt, int Kp,
+                         float* lse_out, float* loss_rows_out, double* block_sums, cudaStream_t s);
+cudaError_t launch_chunk_reduce(const double* block_sums, int nblocks, double* acc, int first, cudaStream_t s);
+cudaError_t launch_finalize(const double* acc, double inv_T, float* loss, cudaStream_t s);
+
+// Top-K (kd_topk.cu).
+size_t topk_smem_bytes(int K);
+cudaError_t launch_topk(const void* logits, int dtype, int64_t T, int64_t V, int64_t ld, int K, int32_t* ids,
+                        float* logp, int* ws_words, int force_exact, int num_sms, cudaStream_t stream);
+
+}  // namespace kd

@@ -1,0 +1,240 @@
+// kd_loss_aux.cu - the per-chunk steps of the fused KL loss that are not GEMMs.
+//
+//  prep    teacher side of the loss for one chunk: p = softmax over the K
+//          cached log-probs (renormalised over K), the entropy term
+//          sum_k p log p, and the (id, p) list sorted by id with duplicates
+//          summed, so that the GEMM epilogues can find the ids inside each
+//          vocabulary tile.
+//  merge   per position: log-sum-exp over the whole vocabulary from the
+//          per-tile (max, sum) partials of the forward GEMM; the loss
+//          L_t = sum p log p - sum_k p_k z_id_k + lse_t; a per-block sum.
+//  reduce  the chunk's block sums, added to the running fp64 total in a fixed
+//          order, and finally loss = total / T.
+// All reductions run in a fixed order, so the loss is bitwise reproducible.
+// Definition: "ทำให้ Knowledge Distillation มีประสิทธิภาพ..." (ai-thai.com),
+// section "กลไก Fused Chunked KL Loss". The KL direction, the
+// renormalisation over K and the mean over positions are this build's
+// readings (the page states no formula).
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kd_internal.h"
+#include "kd_ptx.cuh"
+
+namespace kd {
+namespace {
+
+constexpr int kPrepThreads = 128;
+constexpr uint64_t kDropKey = ~0ull;
+
+__device__ float block_reduce_max(float v, float* sm) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) sm[w] = v;
+  __syncthreads();
+  float r = sm[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r = fmaxf(r, sm[i]);
+  __syncthreads();
+  return r;
+}
+
+// Sum in a fixed order: per-thread strided partial, xor tree, warps in order.
+__device__ float block_reduce_sum(float v, float* sm) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) sm[w] = v;
+  __syncthreads();
+  float r = sm[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r += sm[i];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* __restrict__ ids,
+                                                            const float* __restrict__ logp, int K, int V,
+                                                            int Kp, int Kpow2, int* __restrict__ ids_sorted,
+                                                            float* __restrict__ p_sorted, int* __restrict__ cnt,
+                                                            float* __restrict__ ent, int* status) {
+  extern __shared__ uint64_t keys[];  // [Kpow2]
+  __shared__ float red[kPrepThreads / 32];
+  __shared__ int scan_w[kPrepThreads / 32 + 1];
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const int32_t* rid = ids + (size_t)r * K;
+  const float* rl = logp + (size_t)r * K;
+
+  // Teacher renormalised over its K entries.
+  float mx = -INFINITY;
+  for (int k = tid; k < K; k += kPrepThreads) mx = fmaxf(mx, rl[k]);
+  mx = block_reduce_max(mx, red);
+  float se = 0.f;
+  for (int k = tid; k < K; k += kPrepThreads) se += expf(rl[k] - mx);
+  se = block_reduce_sum(se, red);
+  const float lse_k = mx + logf(se);
+  float e = 0.f;
+  for (int k = tid; k < K; k += kPrepThreads) {
+    const float lp = rl[k] - lse_k;
+    e += expf(lp) * lp;
+  }
+  e = block_reduce_sum(e, red);
+  if (tid == 0) ent[r] = e;
+
+  // Sort (id, original slot) by id; bad ids sort last and are dropped.
+  bool bad = false;
+  for (int i = tid; i < Kpow2; i += kPrepThreads) {
+    uint64_t key = kDropKey;
+    if (i < K) {
+      const int id = rid[i];
+      if (id < 0 || id >= V) bad = true;
+      else key = ((uint64_t)(uint32_t)id << 32) | (uint32_t)i;
+    }
+    keys[i] = key;
+  }
+  if (bad) set_status(status, ST_BAD_ID);
+  __syncthreads();
+  for (int k = 2; k <= Kpow2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < Kpow2; i += kPrepThreads) {
+        const int p = i ^ j;
+        if (p > i) {
+          const uint64_t a = keys[i], b = keys[p];
+          const bool up = (i & k) == 0;
+          if (up ? (a > b) : (a < b)) { keys[i] = b; keys[p] = a; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // Compact runs of equal ids: one output entry per distinct id with the
+  // summed probability (the scatter-add of duplicates).
+  int base_out = 0;
+  for (int base = 0; base < Kpow2; base += kPrepThreads) {
+    const int i = base + tid;
+    const uint64_t key = keys[i];
+    const bool valid = key != kDropKey;
+    const uint32_t id = (uint32_t)(key >> 32);
+    const bool head = valid && (i == 0 || (uint32_t)(keys[i - 1] >> 32) != id || keys[i - 1] == kDropKey);
+    const int lane = tid & 31, w = tid >> 5;
+    const unsigned bal = __ballot_sync(0xffffffffu, head);
+    if (lane == 0) scan_w[w] = __popc(bal);
+    __syncthreads();
+    if (tid == 0) {
+      int acc = 0;
+      for (int q = 0; q < kPrepThreads / 32; ++q) { const int t = scan_w[q]; scan_w[q] = acc; acc += t; }
+      scan_w[kPrepThreads / 32] = acc;
+    }
+    __syncthreads();
+    if (head) {
+      const int slot = base_out + scan_w[w] + __popc(bal & ((1u << lane) - 1u));
+      float ps = 0.f;
+      for (int j = i; j < Kpow2 && keys[j] != kDropKey && (uint32_t)(keys[j] >> 32) == id; ++j)
+        ps += expf(rl[(uint32_t)keys[j]] - lse_k);
+      ids_sorted[(size_t)r * Kp + slot] = (int)id;
+      p_sorted[(size_t)r * Kp + slot] = ps;
+    }
+    base_out += scan_w[kPrepThreads / 32];
+    __syncthreads();
+  }
+  if (tid == 0) cnt[r] = base_out;
+}
+
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) { m = m2; s = s2; return; }
+  const float mm = fmaxf(m, m2);
+  s = s * expf(m - mm) + s2 * expf(m2 - mm);
+  m = mm;
+}
+
+// 256 threads, 32 positions per block: warp w merges vocabulary tiles
+// w, w+8, ... for its 32 positions; warp 0 then merges the 8 results.
+__global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ part_m,
+                                                    const float* __restrict__ part_s, int S, int rows,
+                                                    int row_stride, const float* __restrict__ ent,
+                                                    const float* __restrict__ p_sorted,
+                                                    const float* __restrict__ zK, const int* __restrict__ cnt,
+                                                    int Kp, float* __restrict__ lse_out,
+                                                    float* __restrict__ loss_rows_out,
+                                                    double* __restrict__ block_sums) {
+  __shared__ float sm[8][32], ss[8][32];
+  __shared__ float sl[32];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int row = blockIdx.x * 32 + lane;
+  float m = -INFINITY, s = 0.f;
+  if (row < rows) {
+    for (int j = w; j < S; j += 8) lse_merge(m, s, part_m[(size_t)j * row_stride + row], part_s[(size_t)j * row_stride + row]);
+  }
+  sm[w][lane] = m;
+  ss[w][lane] = s;
+  __syncthreads();
+  if (w == 0) {
+    float M = sm[0][lane], Ssum = ss[0][lane];
+    for (int q = 1; q < 8; ++q) lse_merge(M, Ssum, sm[q][lane], ss[q][lane]);
+    float L = 0.f;
+    if (row < rows) {
+      const float lse = M + logf(Ssum);
+      const int c = cnt[row];
+      float dot = 0.f;
+      for (int k = 0; k < c; ++k) dot += p_sorted[(size_t)row * Kp + k] * zK[(size_t)row * Kp + k];
+      L = ent[row] - dot + lse;
+      lse_out[row] = lse;
+      if (loss_rows_out) loss_rows_out[row] = L;
+    }
+    sl[lane] = L;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    double acc = 0.0;
+    for (int i = 0; i < 32; ++i) acc += (double)sl[i];
+    block_sums[blockIdx.x] = acc;
+  }
+}
+
+__global__ void chunk_reduce_kernel(const double* __restrict__ block_sums, int nblocks, double* acc, int first) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  double s = 0.0;
+  for (int i = 0; i < nblocks; ++i) s += block_sums[i];
+  *acc = first ? s : (*acc + s);
+}
+
+__global__ void finalize_kernel(const double* acc, double inv_T, float* loss) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) *loss = (float)(*acc * inv_T);
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const int32_t* ids, const float* logp, int rows, int K, int V, int Kp, int* ids_sorted,
+                        float* p_sorted, int* cnt, float* ent, int* status, cudaStream_t s) {
+  int Kpow2 = 1;
+  while (Kpow2 < K) Kpow2 <<= 1;
+  if (Kpow2 < kPrepThreads) Kpow2 = kPrepThreads;
+  const size_t smem = (size_t)Kpow2 * sizeof(uint64_t);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  prep_kernel<<<rows, kPrepThreads, smem, s>>>(ids, logp, K, V, Kp, Kpow2, ids_sorted, p_sorted, cnt, ent,
+                                              status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const float* part_m, const float* part_s, int S, int rows, int row_stride,
+                         const float* ent, const float* p_sorted, const float* zK, const int* cnt, int Kp,
+                         float* lse_out, float* loss_rows_out, double* block_sums, cudaStream_t s) {
+  const int nb = (rows + 31) / 32;
+  merge_kernel<<<nb, 256, 0, s>>>(part_m, part_s, S, rows, row_stride, ent, p_sorted, zK, cnt, Kp, lse_out,
+                                  loss_rows_out, block_sums);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_reduce(const double* block_sums, int nblocks, double* acc, int first, cudaStream_t s) {
+  chunk_reduce_kernel<<<1, 32, 0, s>>>(block_sums, nblocks, acc, first);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const double* acc, double inv_T, float* loss, cudaStream_t s) {
+  finalize_kernel<<<1, 32, 0, s>>>(acc, inv_T, loss);
+  return cudaGetLastError();
+}
+
+}  // namespace kd
