@@ -1,0 +1,487 @@
+"""Benchmark: fused top-K KL loss, forward + backward, on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one pass of the whole loss path over one batch: kd_fused_kl_fwd
+(teacher prep, logits GEMM with the online log-sum-exp and id gather in its
+epilogue, merge) and then kd_fused_kl_bwd (recompute GEMM with the dz
+epilogue, dH and dW GEMMs), chunk by chunk. The default workload is the
+Llama-3.2-3B-shaped projection (T=8192, d=3072, V=128256, K=100,
+chunk=1024) with synthetic inputs and a teacher cache built by
+kd_topk_cache from a perturbed-W teacher. The offline cache extraction is
+timed separately on its own workload ([8192, 201088] bf16 logits) and reported
+under "topk_extraction".
+
+Prints one JSON line (rank 0). Under torchrun each rank runs an independent
+replica on its own GPU (no collective on the data path); the barrier and the
+max over ranks use torch.distributed.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import top_kl_loss_tcgen05_b300 as kd  # noqa: E402
+from top_kl_loss_tcgen05_b300 import _native, synth  # noqa: E402
+
+METRIC = "fused top-K KL fwd+bwd tokens/s and TFLOP/s (% BF16 tensor peak); peak GiB"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_src_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "top_kl_loss_tcgen05_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources and this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("src_sha") != kernel_src_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev: torch.device):
+        self.uuid = None
+        try:
+            self.uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+        except Exception:
+            pass
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+# ----------------------------------------------------------------------------- workload
+
+
+def make_workload(name: str, dev: torch.device):
+    c = synth.CONFIGS[name]
+    T, d, V, K, chunk, seed = c["T"], c["d"], c["V"], c["K"], c["chunk"], c["seed"]
+    H, W = synth.student(T, d, V, seed, device=dev)
+    # teacher cache: perturbed-W teacher logits (fp32, chunk by chunk) -> kd_topk_cache
+    Wt = synth.teacher_weight(W, seed)
+    ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+    logp = torch.empty(T, K, dtype=torch.float32, device=dev)
+    step = max(1, min(T, (1 << 30) // (4 * V)))
+    for t0 in range(0, T, step):
+        t1 = min(T, t0 + step)
+        tl = synth.teacher_logits_from(H[t0:t1], Wt)
+        i, lp = kd.topk_cache(tl, K)
+        ids[t0:t1] = i
+        logp[t0:t1] = lp
+        del tl
+    del Wt
+    torch.cuda.synchronize(dev)
+    return dict(T=T, d=d, V=V, K=K, chunk=chunk, H=H, W=W, ids=ids, logp=logp)
+
+
+def describe(name: str) -> str:
+    c = synth.CONFIGS[name]
+    return "%s: T=%d d=%d V=%d K=%d chunk=%d" % (name, c["T"], c["d"], c["V"], c["K"], c["chunk"])
+
+
+# ----------------------------------------------------------------------------- oracle (cpu baseline)
+
+
+def oracle_sample(wl_cpu, rows: int):
+    """Time the fp64 oracle on `rows` positions of the workload (fwd + bwd)."""
+    from oracle import kd_oracle as O
+
+    H = wl_cpu["H"][:rows]
+    W64 = wl_cpu["W64"]
+    ids = wl_cpu["ids"][:rows]
+    logp = wl_cpu["logp"][:rows]
+    t0 = time.perf_counter()
+    O.fused_kl_forward(H, W64, ids, logp)
+    O.fused_kl_backward(H, W64, ids, logp, 1.0 / wl_cpu["T"])
+    return time.perf_counter() - t0
+
+
+def cpu_workload(wl):
+    return dict(T=wl["T"], H=wl["H"][:4096].float().cpu().numpy().astype(np.float64),
+                W64=wl["W"].float().cpu().numpy().astype(np.float64), ids=wl["ids"][:4096].cpu().numpy(),
+                logp=wl["logp"][:4096].cpu().numpy())
+
+
+def cpu_baseline(wl, budget_s: float = 15.0):
+    cw = cpu_workload(wl)
+    t1 = oracle_sample(cw, 2)
+    rows = int(max(2, min(4096, budget_s / max(t1 / 2, 1e-6))))
+    t = oracle_sample(cw, rows)
+    return {"value": rows / t, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": "fp64 numpy oracle, forward + backward (loss, lse, dH, dW contribution) of the first %d "
+                      "positions of the workload at full d and V; %.1f s" % (rows, t)}
+
+
+# ----------------------------------------------------------------------------- top-K extraction
+
+
+def bench_topk(dev, peaks, iters=5):
+    c = synth.CONFIGS["topk"]
+    x = synth.topk_logits(c["T"], c["V"], c["seed"], device=dev)
+    ws = kd.workspace(256, dev)
+    for _ in range(2):
+        kd.topk_cache(x, c["K"], ws=ws)
+    torch.cuda.synchronize(dev)
+    _native.profile_begin()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(iters):
+        kd.topk_cache(x, c["K"], ws=ws)
+    e.record()
+    torch.cuda.synchronize(dev)
+    prof = _native.profile_end()
+    ms = s.elapsed_time(e) / iters
+    launches, kms = prof.get("topk_cache", (iters, ms * iters))
+    kernel_ms = kms / max(1, launches)
+    nbytes = 2 * c["T"] * c["V"] + 8 * c["T"] * c["K"]
+    achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    fallback_rows = int(ws[4:8].view(torch.int32).item())
+    del x
+    return {
+        "workload": "topk: logits [%d, %d] bf16 (N(0,2) + Zipf-like bias), K=%d" % (c["T"], c["V"], c["K"]),
+        "ms": kernel_ms, "rows_per_s": c["T"] / (kernel_ms * 1e-3),
+        "rows_on_radix_path": fallback_rows // (iters + 2),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": ncu_traffic("topk_cache", "topk"), "algorithmic_bytes_per_launch": nbytes},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    name = args.workload
+    c = synth.CONFIGS[name]
+    # inputs drawn exactly as for the GPU arm (the cache from the synthetic
+    # perturbed teacher is not needed to time the oracle: a synthetic cache of
+    # the same shape is used so this arm runs without the GPU path)
+    H, W = synth.student(min(c["T"], 4096), c["d"], c["V"], c["seed"], device="cpu")
+    ids, logp = synth.synthetic_cache(min(c["T"], 4096), c["V"], c["K"], c["seed"])
+    cw = dict(T=c["T"], H=H.float().numpy().astype(np.float64), W64=W.float().numpy().astype(np.float64),
+              ids=ids.numpy(), logp=logp.numpy())
+    t1 = oracle_sample(cw, 2)
+    rows = int(max(2, min(4096, 8.0 / max(t1 / 2, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_sample(cw, 2)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(cw, rows)
+    el = time.perf_counter() - t0
+    value = rows * args.steps / el
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(name), "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "fp64 numpy oracle fwd+bwd of %d positions per step at full d and V" % rows},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama3b", choices=["tiny", "llama3b", "gptoss20b", "long"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-topk", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    dev = torch.device("cuda", local)
+    peaks, peaks_src = load_peaks()
+    _native.load()
+
+    wl = make_workload(args.workload, dev)
+    T, d, V, K, chunk = wl["T"], wl["d"], wl["V"], wl["K"], wl["chunk"]
+    H, W, ids, logp = wl["H"], wl["W"], wl["ids"], wl["logp"]
+    ws = kd.fused_kl_workspace(d, V, K, chunk, dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    dH = torch.empty(T, d, dtype=torch.float32, device=dev)
+    dW = torch.empty(V, d, dtype=torch.float32, device=dev)
+    L = _native.lib()
+    stream = torch.cuda.current_stream(dev).cuda_stream
+
+    def step(Hx=H, idsx=ids, logpx=logp):
+        _native.check("kd_fused_kl_fwd", L.kd_fused_kl_fwd(
+            Hx.data_ptr(), W.data_ptr(), idsx.data_ptr(), logpx.data_ptr(), T, d, V, K, chunk, loss.data_ptr(),
+            lse.data_ptr(), None, ws.data_ptr(), ws.numel(), stream))
+        _native.check("kd_fused_kl_bwd", L.kd_fused_kl_bwd(
+            Hx.data_ptr(), W.data_ptr(), idsx.data_ptr(), logpx.data_ptr(), lse.data_ptr(), T, d, V, K, chunk,
+            1.0 / T, None, dH.data_ptr(), dW.data_ptr(), 0, ws.data_ptr(), ws.numel(), stream))
+
+    # peak device memory of one step (everything is allocated through torch)
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    step()
+    torch.cuda.synchronize(dev)
+    peak_gib = torch.cuda.max_memory_allocated(dev) / 2**30
+    ws_gib = ws.numel() / 2**30
+    for _ in range(args.warmup - 1):
+        step()
+    torch.cuda.synchronize(dev)
+    status = kd.read_device_status(ws)
+    if status != 0:
+        raise RuntimeError("device status %s during warm-up" % _native.status_string(status))
+
+    # ---- timed region (device-resident inputs)
+    clocks = ClockSampler(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    _native.profile_begin()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(args.steps):
+        step()
+    ev1.record()
+    torch.cuda.synchronize(dev)
+    prof = _native.profile_end()
+    barrier(world)
+    clk = clocks.stop()
+    el_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    ms_step = el_ms / args.steps
+    tokens_s = T * args.steps * world / (el_ms * 1e-3)
+    flops_step = 8.0 * T * d * V
+    tflops = flops_step * args.steps * world / (el_ms * 1e-3) / 1e12
+    peak_tf = float(peaks["bf16_tflops_sustained"])
+    status = kd.read_device_status(ws)
+    if status != 0:
+        raise RuntimeError("device status %s in the timed region" % _native.status_string(status))
+
+    # dominant kernel and its roofline (algorithmic flops per launch / mean launch time)
+    nchunks = (T + chunk - 1) // chunk
+    flops_per_launch = {"logits_fwd_lse_gather": 2.0 * T * d * V / nchunks,
+                        "logits_dz": 2.0 * T * d * V / nchunks,
+                        "grad_dH_dW": 4.0 * T * d * V / nchunks}
+    total_kernel_ms = sum(v[1] for v in prof.values())
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
+    kernels = {k: {"launches": n, "ms_per_step": t / args.steps, "share": t / total_kernel_ms if total_kernel_ms else 0.0}
+               for k, (n, t) in prof.items()}
+    roof = None
+    if dom in flops_per_launch:
+        n, t = prof[dom]
+        achieved = flops_per_launch[dom] / (t / n * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf, "traffic": ncu_traffic(dom, args.workload), "kernel": dom,
+                "peak_kind": "bf16_tflops_sustained (%s)" % peaks_src,
+                "algorithmic_flops_per_launch": flops_per_launch[dom]}
+    for k in kernels:
+        if k in flops_per_launch:
+            n, t = prof[k]
+            kernels[k]["tflops"] = flops_per_launch[k] / (t / n * 1e-3) / 1e12
+    gpu_launches = sum(n for n, _ in prof.values())
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        Hh = H.cpu().pin_memory()
+        ih = ids.cpu().pin_memory()
+        lh = logp.cpu().pin_memory()
+        Hd = torch.empty_like(H)
+        idd = torch.empty_like(ids)
+        ld = torch.empty_like(logp)
+        out = torch.empty((), dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            Hd.copy_(Hh, non_blocking=True)
+            idd.copy_(ih, non_blocking=True)
+            ld.copy_(lh, non_blocking=True)
+            step(Hd, idd, ld)
+            out.copy_(loss, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+            return float(out)
+
+        for _ in range(2):
+            e2e_step()
+        barrier(world)
+        n_e2e = max(3, args.steps // 2)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        el = max_over_ranks(time.perf_counter() - t0, world)
+        bi = Hh.numel() * Hh.element_size() + ih.numel() * 4 + lh.numel() * 4
+        e2e = {"value": T * n_e2e * world / el, "unit": "tokens/s", "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": 4, "steps": n_e2e,
+               "note": "H, teacher ids and logp copied from pinned host memory every step, loss read back; "
+                       "W (LM-head parameter), dH and dW stay on the device"}
+
+    topk = None if args.no_topk else bench_topk(dev, peaks)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "tflops": tflops, "pct_bf16_peak": tflops / peak_tf,
+            "pct_bf16_peak_basis": "8*T*d*V flops per step vs bf16_tflops_sustained (%s)" % peaks_src,
+            "peak_gib": peak_gib, "workspace_gib": ws_gib,
+            "config": {"workload": describe(args.workload), "parallelism": "replicas" if world > 1 else "1 gpu",
+                       "l2": "inputs larger than L2 (W alone is %.0f MB)" % (V * d * 2 / 1e6),
+                       "teacher_cache": "kd_topk_cache of fp32 perturbed-W teacher logits"},
+            "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
+            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "topk_extraction": topk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -27,6 +27,8 @@ import torch
 __all__ = [
     "CONFIGS",
     "student",
+    "teacher_weight",
+    "teacher_logits_from",
     "teacher_logits",
     "topk_logits",
     "synthetic_cache",
@@ -61,19 +63,28 @@ def student(T: int, d: int, V: int, seed: int, device="cpu"):
     return H, W
 
 
+def teacher_weight(W: torch.Tensor, seed: int) -> torch.Tensor:
+    """fp32 perturbed teacher projection W + E with E ~ N(0, 0.5/d)."""
+    V, d = W.shape
+    g = _gen(seed + 7919, W.device)
+    E = torch.randn(V, d, generator=g, device=W.device, dtype=torch.float32) * math.sqrt(0.5 / d)
+    return W.float() + E
+
+
+def teacher_logits_from(Hs: torch.Tensor, Wt: torch.Tensor) -> torch.Tensor:
+    """fp32 teacher logits 1.5 * Hs Wt^T for a block of positions."""
+    with _no_tf32():
+        return 1.5 * (Hs.float() @ Wt.T)
+
+
 def teacher_logits(H: torch.Tensor, W: torch.Tensor, seed: int, rows: slice | None = None):
     """fp32 teacher logits 1.5 * H (W + E)^T with E ~ N(0, 0.5/d).
 
     E is drawn for the whole of W from `seed`, so the same teacher serves
     every row. `rows` restricts the output to those positions.
     """
-    V, d = W.shape
-    g = _gen(seed + 7919, W.device)
-    E = torch.randn(V, d, generator=g, device=W.device, dtype=torch.float32) * math.sqrt(0.5 / d)
-    Wt = W.float() + E
     Hs = H if rows is None else H[rows]
-    with _no_tf32():
-        return 1.5 * (Hs.float() @ Wt.T)
+    return teacher_logits_from(Hs, teacher_weight(W, seed))
 
 
 class _no_tf32:
