@@ -107,6 +107,27 @@ KD_API int kd_topk_cache(const void* logits, int32_t dtype, int64_t T, int64_t V
                   int32_t K, int32_t* ids, float* logp, void* ws, size_t ws_bytes,
                   void* stream);
 
+/* kd_topk_cache_noalloc: the same extraction, for callers that cannot
+ * allocate device memory and so cannot pass a workspace. Examples: a step
+ * running inside a host application that owns every device allocation
+ * through its own pool, or a loop that cannot accept cudaMalloc's implicit
+ * synchronisation. The paper has no counterpart; this is a library
+ * convenience. Arguments are those of kd_topk_cache without ws/ws_bytes.
+ * Scratch comes from a fixed 4096-byte array in device memory owned by
+ * libkd. Every GPU that loads the library holds it until the process exits.
+ * The call allocates nothing.
+ *  - The first call on a device looks up that array's device address
+ *    (cudaGetSymbolAddress). Make that first call before any stream capture.
+ *  - Each call clears the array on `stream`. Calls that overlap on the GPU
+ *    (unordered streams) share the array and race on it.
+ *  - If the workspace that kd_topk_cache would need exceeds the array, the call
+ *    returns KD_ERR_WORKSPACE (it never does for the current kernel, which
+ *    needs 256 bytes).
+ *  - A device-side status cannot be read back afterwards; use kd_topk_cache
+ *    with your own workspace when you need it. */
+KD_API int kd_topk_cache_noalloc(const void* logits, int32_t dtype, int64_t T, int64_t V,
+                                 int64_t ld, int32_t K, int32_t* ids, float* logp, void* stream);
+
 /* ------------------------------------------------------------ fused KL loss
  *
  * Shared arguments:

@@ -33,6 +33,7 @@ SIGNATURES = {
     "kd_version": (ctypes.c_int, []),
     "kd_topk_workspace_size": (_SZ, [_I64, _I64, _I32, _I32]),
     "kd_topk_cache": (ctypes.c_int, [_P, _I32, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
+    "kd_topk_cache_noalloc": (ctypes.c_int, [_P, _I32, _I64, _I64, _I64, _I32, _P, _P, _P]),
     "kd_fused_kl_workspace_size": (_SZ, [_I64, _I64, _I32, _I64]),
     "kd_fused_kl_fwd": (
         ctypes.c_int,

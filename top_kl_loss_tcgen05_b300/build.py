@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libkd.so")
 
-SOURCES = ["kd_api.cu", "kd_gemm.cu", "kd_topk.cu", "kd_loss_aux.cu"]
+SOURCES = ["kd_api.cu", "kd_gemm.cu", "kd_topk.cu", "kd_loss_aux.cu", "kd_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-Xcompiler", "-fvisibility=hidden"]
 
