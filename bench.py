@@ -217,8 +217,10 @@ def cpu_baseline(wl, budget_s: float = 15.0):
 # ----------------------------------------------------------------------------- top-K extraction
 
 
-def bench_topk(dev, peaks, iters=5):
-    c = synth.CONFIGS["topk"]
+def bench_topk(dev, peaks, iters=5, rows=None):
+    c = dict(synth.CONFIGS["topk"])
+    if rows:
+        c["T"] = int(rows)
     x = synth.topk_logits(c["T"], c["V"], c["seed"], device=dev)
     ws = kd.workspace(256, dev)
     for _ in range(2):
@@ -331,6 +333,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-topk", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--topk-rows", type=int, default=None, help="rows of the top-K workload (default 8192)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup(args)
@@ -457,7 +460,7 @@ def main():
                "note": "H, teacher ids and logp copied from pinned host memory every step, loss read back; "
                        "W (LM-head parameter), dH and dW stay on the device"}
 
-    topk = None if args.no_topk else bench_topk(dev, peaks)
+    topk = None if args.no_topk else bench_topk(dev, peaks, rows=args.topk_rows)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)

@@ -13,17 +13,18 @@
 extern "C" {
 #endif
 
-/* C[M, N] (fp32, row-major, device) = A * B^T on the tcgen05 GEMM that the
- * backward pass uses for dH and dW (128 x 192 tiles, TMA loads, TMEM
- * accumulators, TMA store or TMA reduce-add epilogue).
+/* C = A * B^T (fp32, row-major, device) on the tcgen05 GEMM that the
+ * backward pass uses for dH and dW (128 x 256 tiles, dynamic tile
+ * scheduling, TMA loads, TMEM accumulators, TMA store / reduce-add).
  *   A: a_mn == 0 -> [M, K] row-major; a_mn == 1 -> [K, M] row-major (bf16).
  *   B: b_mn == 0 -> [N, K] row-major; b_mn == 1 -> [K, N] row-major (bf16).
- *   reduce_add != 0 adds into C instead of overwriting it.
- * Requires K, and M or N for MN-major operands, to be multiples of 8;
- * C's N a multiple of 4. `ws` (>= 256 bytes, device) receives the status word.
- * Returns a kd_status value. */
+ *   flags bit 0: add into C instead of overwriting it.
+ *   flags bit 1: store C transposed, i.e. C is [N, M] row-major.
+ * Requires K, and M or N for MN-major operands, to be multiples of 8, and
+ * C's row length a multiple of 4. `ws` (>= 256 bytes, device) holds the
+ * status word and the tile counter. Returns a kd_status value. */
 KD_API int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int32_t a_mn,
-                 int32_t b_mn, int32_t reduce_add, void* ws, void* stream);
+                        int32_t b_mn, int32_t flags, void* ws, void* stream);
 
 #ifdef __cplusplus
 }

@@ -11,21 +11,25 @@ from top_kl_loss_tcgen05_b300 import _native, workspace
 pytestmark = pytest.mark.gpu
 
 
-def _run(M, N, K, a_mn, b_mn, reduce_add=False, seed=0):
+def _run(M, N, K, a_mn, b_mn, reduce_add=False, seed=0, c_trans=False):
     dev = torch.device("cuda:0")
     g = torch.Generator(device=dev).manual_seed(seed)
     A = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
     B = torch.randn(N, K, generator=g, device=dev).to(torch.bfloat16)
     Ain = A.t().contiguous() if a_mn else A.contiguous()
     Bin = B.t().contiguous() if b_mn else B.contiguous()
-    C0 = torch.randn(M, N, generator=g, device=dev) if reduce_add else torch.full((M, N), float("nan"), device=dev)
+    shape = (N, M) if c_trans else (M, N)
+    C0 = torch.randn(*shape, generator=g, device=dev) if reduce_add else torch.full(shape, float("nan"), device=dev)
     C = C0.clone()
     ws = workspace(256, dev)
+    flags = (1 if reduce_add else 0) | (2 if c_trans else 0)
     rc = _native.lib().kd_test_gemm(Ain.data_ptr(), Bin.data_ptr(), C.data_ptr(), M, N, K, a_mn, b_mn,
-                                    1 if reduce_add else 0, ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+                                    flags, ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert rc == 0, _native.status_string(rc)
     assert _native.lib().kd_read_device_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
     ref = A.double() @ B.double().t()
+    if c_trans:
+        ref = ref.t()
     if reduce_add:
         ref = ref + C0.double()
     err = (C.double() - ref).norm() / ref.norm()
@@ -53,3 +57,13 @@ def test_gemm_many_tiles_persistent(cuda_dev):
     # more tiles than SMs: every CTA loops over several tiles and both TMEM
     # accumulators
     _run(128 * 40, 192 * 9, 128, 0, 1, seed=4)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(1, 0), (0, 0), (1, 1)])
+def test_gemm_transposed_store(cuda_dev, a_mn, b_mn):
+    _run(264, 1000, 520, a_mn, b_mn, seed=5, c_trans=True)
+    _run(3072, 1024, 4096, a_mn, b_mn, seed=6, c_trans=True)
+
+
+def test_gemm_transposed_reduce_add(cuda_dev):
+    _run(136, 520, 64, 1, 0, reduce_add=True, seed=7, c_trans=True)

@@ -32,6 +32,7 @@ namespace kd {
 namespace {
 
 constexpr size_t kHeader = 256;  // status word, counters, fp64 loss accumulator
+constexpr size_t kCounterOffset = 64;  // int: tile counter of the GEMM launches
 constexpr size_t kAccOffset = 128;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -61,15 +62,16 @@ struct Layout {
   int Kp;
   int64_t S;    // vocabulary tiles of the forward GEMM
   int64_t ldz;  // dz row stride in elements
-  size_t ids_sorted, p_sorted, cnt, ent, zK, block_sums, part_m, part_s, dz, total;
+  int64_t ldt;  // row stride of the transposed hidden-state chunk
+  size_t ids_sorted, p_sorted, cnt, ent, zK, block_sums, part_m, part_s, hct, dz, total;
 };
 
 Layout fused_layout(int64_t d, int64_t V, int K, int64_t chunk) {
-  (void)d;
   Layout L;
   L.Kp = (K + 3) / 4 * 4;
   L.S = ceil_div(V, kBNLogits);
   L.ldz = align_up((size_t)V, 64);
+  L.ldt = align_up((size_t)chunk, 64);
   size_t o = kHeader;
   auto take = [&](size_t bytes, size_t al) {
     o = align_up(o, al);
@@ -85,6 +87,7 @@ Layout fused_layout(int64_t d, int64_t V, int K, int64_t chunk) {
   L.block_sums = take((size_t)ceil_div(chunk, 32) * 8, 256);
   L.part_m = take((size_t)L.S * chunk * 4, 256);
   L.part_s = take((size_t)L.S * chunk * 4, 256);
+  L.hct = take((size_t)d * L.ldt * 2, 1024);
   L.dz = take((size_t)chunk * L.ldz * 2, 1024);
   L.total = align_up(o, 256);
   return L;
@@ -94,10 +97,12 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // ------------------------------------------------------------------ profiling
 // Kernel names reported by kd_profile_end, indexed by KernelId.
-enum KernelId { K_TOPK, K_PREP, K_LOGITS_FWD, K_MERGE, K_REDUCE, K_FINALIZE, K_LOGITS_DZ, K_GRAD, K_TEST, K_COUNT };
+enum KernelId {
+  K_TOPK, K_PREP, K_LOGITS_FWD, K_MERGE, K_REDUCE, K_FINALIZE, K_LOGITS_DZ, K_TRANSPOSE, K_GRAD, K_TEST, K_COUNT
+};
 const char* const kKernelNames[K_COUNT] = {"topk_cache", "teacher_prep", "logits_fwd_lse_gather", "lse_merge_loss",
-                                           "loss_chunk_reduce", "loss_finalize", "logits_dz", "grad_dH_dW",
-                                           "test_gemm"};
+                                           "loss_chunk_reduce", "loss_finalize", "logits_dz", "hidden_transpose",
+                                           "grad_dH_dW", "test_gemm"};
 struct ProfRec {
   int kid;
   cudaEvent_t a, b;
@@ -271,6 +276,7 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
     a.ids_sorted = ids_sorted; a.p_sorted = p_sorted; a.cnt = cnt;
     a.zK = zK; a.part_m = part_m; a.part_s = part_s;
     a.status = status;
+    a.tile_counter = reinterpret_cast<int*>(w + kCounterOffset);
     {
       ProfScope ps(K_LOGITS_FWD, s);
       e = launch_logits_fwd(a, sms, s);
@@ -316,12 +322,14 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
   GemmArgs az, ag;
   std::memset(&az, 0, sizeof(az));
   std::memset(&ag, 0, sizeof(ag));
+  int* counter = reinterpret_cast<int*>(w + kCounterOffset);
+  __nv_bfloat16* hct = reinterpret_cast<__nv_bfloat16*>(w + L.hct);
   cudaError_t e;
-  // W as the K-major B of the logits GEMM and the N-major B of dH.
+  // W: K-major B of the logits GEMM, M-major A of the dH^T GEMM.
   e = encode_map_2d(&az.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2,
                     kBK, kBNLogits);
   if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
-  e = encode_map_2d(&ag.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, 64,
+  e = encode_map_2d(&ag.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, 64,
                     64);
   if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
   e = encode_map_2d(&ag.tmC[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, (uint64_t)d, (uint64_t)V, (uint64_t)d * 4, 32,
@@ -348,13 +356,14 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
       P.n_blocks = (int)ceil_div(V, kBNLogits);
       P.k_blocks = (int)ceil_div(d, kBK);
       P.a_mn = 0; P.b_mn = 0; P.M = rows; P.N = (int)V;
-      P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0;
+      P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
       az.nprob = 1;
       az.total_tiles = P.m_blocks * P.n_blocks;
       az.rows = rows; az.row_stride = (int)chunk; az.V = (int)V; az.Kp = L.Kp;
       az.ids_sorted = ids_sorted; az.p_sorted = p_sorted; az.cnt = cnt;
       az.lse = lse + c0; az.scale = grad_scale; az.dscale = grad_scale_dev;
       az.status = status;
+      az.tile_counter = counter;
     }
     {
       ProfScope ps(K_LOGITS_DZ, s);
@@ -362,33 +371,43 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
     }
     if (e != cudaSuccess) return cuda_status(e);
 
-    // dH_c = dz W (problem 0) and dW (+)= dz^T H_c (problem 1), one launch.
-    if (encode_map_2d(&ag.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)rows,
-                      (uint64_t)L.ldz * 2, kBK, kBM) != cudaSuccess ||
+    // H_c^T [d, rows] (K-major B operand of the dW GEMM).
+    {
+      ProfScope ps(K_TRANSPOSE, s);
+      e = launch_transpose(Hb + c0 * d, rows, (int)d, hct, (int)L.ldt, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+
+    // dH_c^T = W^T dz^T (problem 0, stored transposed into dH) and
+    // dW (+)= dz^T H_c (problem 1), one launch.
+    if (encode_map_2d(&ag.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)rows,
+                      (uint64_t)L.ldz * 2, kBK, kBNGrad) != cudaSuccess ||
         encode_map_2d(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dH + c0 * d, (uint64_t)d, (uint64_t)rows,
                       (uint64_t)d * 4, 32, 32) != cudaSuccess ||
         encode_map_2d(&ag.tmA[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)rows,
                       (uint64_t)L.ldz * 2, 64, 64) != cudaSuccess ||
-        encode_map_2d(&ag.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + c0 * d, (uint64_t)d, (uint64_t)rows,
-                      (uint64_t)d * 2, 64, 64) != cudaSuccess)
+        encode_map_2d(&ag.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, hct, (uint64_t)rows, (uint64_t)d,
+                      (uint64_t)L.ldt * 2, kBK, kBNGrad) != cudaSuccess)
       return KD_ERR_UNSUPPORTED;
     {
       Problem& P0 = ag.pr[0];
-      P0.m_blocks = (int)ceil_div(rows, kBM);
-      P0.n_blocks = (int)ceil_div(d, kBNGrad);
+      P0.m_blocks = (int)ceil_div(d, kBM);
+      P0.n_blocks = (int)ceil_div(rows, kBNGrad);
       P0.k_blocks = (int)ceil_div(V, kBK);
-      P0.a_mn = 0; P0.b_mn = 1; P0.M = rows; P0.N = (int)d;
-      P0.tile_begin = 0; P0.n_fastest = 0; P0.reduce_add = 0;
+      P0.a_mn = 1; P0.b_mn = 0; P0.M = (int)d; P0.N = rows;
+      P0.tile_begin = 0; P0.n_fastest = 0; P0.reduce_add = 0; P0.c_trans = 1;
       Problem& P1 = ag.pr[1];
       P1.m_blocks = (int)ceil_div(V, kBM);
       P1.n_blocks = (int)ceil_div(d, kBNGrad);
       P1.k_blocks = (int)ceil_div(rows, kBK);
-      P1.a_mn = 1; P1.b_mn = 1; P1.M = (int)V; P1.N = (int)d;
+      P1.a_mn = 1; P1.b_mn = 0; P1.M = (int)V; P1.N = (int)d;
       P1.tile_begin = P0.m_blocks * P0.n_blocks; P1.n_fastest = 1;
       P1.reduce_add = (accumulate_dW || c0 > 0) ? 1 : 0;
+      P1.c_trans = 0;
       ag.nprob = 2;
       ag.total_tiles = P1.tile_begin + P1.m_blocks * P1.n_blocks;
       ag.status = status;
+      ag.tile_counter = counter;
     }
     {
       ProfScope ps(K_GRAD, s);
@@ -410,9 +429,11 @@ int kd_read_device_status(void* ws, void* stream) {
 }
 
 int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int32_t a_mn,
-                 int32_t b_mn, int32_t reduce_add, void* ws, void* stream) {
+                 int32_t b_mn, int32_t flags, void* ws, void* stream) {
   if (!A || !B || !C || !ws || M <= 0 || N <= 0 || K <= 0) return KD_ERR_INVALID_ARG;
-  if (K % 8 || (a_mn && M % 8) || (b_mn && N % 8) || N % 4) return KD_ERR_UNSUPPORTED;
+  const int reduce_add = flags & 1, c_trans = (flags >> 1) & 1;
+  const int64_t ldc = c_trans ? M : N;  // C is [M, N], or [N, M] when stored transposed
+  if (K % 8 || (a_mn && M % 8) || (b_mn && N % 8) || ldc % 4) return KD_ERR_UNSUPPORTED;
   if (M >= (1 << 30) || N >= (1 << 30) || K >= (1 << 30)) return KD_ERR_UNSUPPORTED;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
@@ -422,7 +443,8 @@ int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, i
                         : encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, kBK, kBM);
   cudaError_t e2 = b_mn ? encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, N * 2, 64, 64)
                         : encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, K * 2, kBK, kBNGrad);
-  cudaError_t e3 = encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, 32);
+  cudaError_t e3 = c_trans ? encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, M, N, M * 4, 32, 32)
+                           : encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, 32);
   if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return KD_ERR_UNSUPPORTED;
   Problem& P = a.pr[0];
   P.m_blocks = (int)ceil_div(M, kBM);
@@ -430,10 +452,11 @@ int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   P.k_blocks = (int)ceil_div(K, kBK);
   P.a_mn = a_mn ? 1 : 0; P.b_mn = b_mn ? 1 : 0;
   P.M = (int)M; P.N = (int)N;
-  P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = reduce_add ? 1 : 0;
+  P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = reduce_add; P.c_trans = c_trans;
   a.nprob = 1;
   a.total_tiles = P.m_blocks * P.n_blocks;
   a.status = static_cast<int*>(ws);
+  a.tile_counter = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + kCounterOffset);
   ProfScope ps(K_TEST, static_cast<cudaStream_t>(stream));
   return cuda_status(launch_grad(a, sms, static_cast<cudaStream_t>(stream)));
 }

@@ -5,11 +5,17 @@
 // states -> logits per chunk, loss accumulated, chunk discarded; backward
 // recomputes each chunk):
 //   logits  z = H_c W^T    A = H_c [c, d] K-major, B = W [V, d] K-major
-//   dH      dz W           A = dz [c, V] K-major,  B = W [V, d] N-major
-//   dW      dz^T H_c       A = dz [c, V] M-major,  B = H_c [c, d] N-major
+//   dH^T    W^T dz^T       A = W [V, d] M-major,   B = dz [c, V] K-major
+//           (stored transposed by the epilogue, so dH lands row-major)
+//   dW      dz^T H_c       A = dz [c, V] M-major,  B = H_c^T [d, c] K-major
+// These are the operand layouts the tensor core reads at full rate (an
+// N-major B costs 15-28% on B300; an M-major A costs nothing).
 // All run in one persistent, warp-specialised kernel template:
-//   warp 0     TMA producer: one thread streams A/B tiles into a ring of
-//              shared-memory stages (128-byte swizzle).
+//   warp 0     TMA producer: one thread takes the next tile from a global
+//              counter (dynamic scheduling), passes its id to the other
+//              roles through a 4-deep shared-memory queue, and streams the
+//              tile's A/B blocks into a ring of shared-memory stages
+//              (128-byte swizzle).
 //   warp 1     MMA issuer: one thread issues tcgen05.mma (M=128, N=BN,
 //              K=16) into one of two TMEM accumulators. tcgen05.commit frees
 //              the smem stage, and then signals the finished accumulator.
@@ -19,7 +25,8 @@
 //     EPI_FWD   online (max, sum exp) per row over the tile's vocabulary
 //               slice, and the logits at the teacher ids that fall in it;
 //     EPI_DZ    dz = s (exp(z - lse) - p [j in K]) -> bf16 -> TMA store;
-//     EPI_GRAD  fp32 tile -> TMA store (dH) or TMA reduce-add (dW += ...).
+//     EPI_GRAD  fp32 tile -> TMA store or TMA reduce-add (dW += ...),
+//               optionally transposed (dH).
 // The logits tile therefore never leaves the chip in the forward pass. In
 // backward, only the chunk's dz (bf16, c x V) goes to HBM.
 #include <cstdint>
@@ -95,8 +102,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint64_t* tfull = bars + 2 * NS;    // [2]  MMA -> epilogue
   uint64_t* tempty = bars + 2 * NS + 2;  // [2] epilogue -> MMA
   uint64_t* drain = bars + 2 * NS + 4;   // MMA drain on abort
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NS + 5);
+  uint64_t* tqf = bars + 2 * NS + 5;     // [4] tile queue: producer -> MMA + epilogue
+  uint64_t* tqe = bars + 2 * NS + 9;     // [4] tile queue: slot free again
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NS + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* tq = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [4] tile ids
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -104,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
     mbar_init(drain, 1);
+    for (int q = 0; q < 4; ++q) { mbar_init(&tqf[q], 1); mbar_init(&tqe[q], 5); }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -130,7 +141,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       uint32_t phase = 0;
       uint32_t issued = 0, ipar = 0;  // per-stage bit: load issued / its phase parity
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < g.total_tiles; t += gridDim.x) {
+      // Tiles are handed out in index order by a global counter: a CTA takes
+      // the next tile when it starts one, so long and short tiles balance.
+      for (int j = 0; ok; ++j) {
+        int t = atomicAdd(g.tile_counter, 1);
+        if (t >= g.total_tiles) t = -1;
+        const int qs = j & 3;
+        if (!mbar_wait(&tqe[qs], ((uint32_t)(j >> 2) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+        tq[qs] = t;
+        mbar_arrive(&tqf[qs]);
+        if (t < 0) break;
         const Tile tl = decode(g, t);
         const Problem& P = g.pr[tl.prob];
         const CUtensorMap* mA = &g.tmA[tl.prob];
@@ -183,7 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < g.total_tiles; t += gridDim.x) {
+      for (int j = 0; ok; ++j) {
+        const int qs = j & 3;
+        if (!mbar_wait(&tqf[qs], (uint32_t)(j >> 2) & 1u, abort_flag)) { ok = false; break; }
+        const int t = tq[qs];
+        mbar_arrive(&tqe[qs]);
+        if (t < 0) break;
         const Tile tl = decode(g, t);
         const Problem& P = g.pr[tl.prob];
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
@@ -230,7 +255,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     int buf = 0, nstore = 0;
     bool ok = true;
     uint8_t* stg = smem + NS * C::STAGE + (uint32_t)wq * 2u * kStageBytesStaging;
-    for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
+    for (int j = 0;; ++j) {
+      const int qs = j & 3;
+      if (!mbar_wait(&tqf[qs], (uint32_t)(j >> 2) & 1u, abort_flag)) ok = false;
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const int t = tq[qs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tqe[qs]);
+      if (t < 0) break;
       const Tile tl = decode(g, t);
       const Problem& P = g.pr[tl.prob];
       const int row_l = 32 * wq + lane;
@@ -367,6 +400,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
+      } else if (P.c_trans) {
+        // C is stored transposed: TMEM lane = column of C, TMEM column = row
+        // of C. Each warp stages a 32 x 32 block as [C row][C column] with
+        // one 4-byte store per element (conflict-free under the 128-byte
+        // swizzle) and stores it with one TMA box.
+        const CUtensorMap* mC = &g.tmC[tl.prob];
+        const bool box_live = tl.mb * kBM + 32 * wq < P.M;
+        for (int c0 = 0; c0 < BN && n0 + c0 < P.N; c0 += 32) {
+          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
+          if (nstore >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+          uint32_t v[32];
+          tmem_ld32(taddr + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int r = 0; r < 32; ++r)
+            st_shared_b32(sb + r * 128 + ((((uint32_t)lane >> 2) ^ (uint32_t)(r & 7)) << 4) + ((lane & 3) << 2), v[r]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && box_live) {
+            if (P.reduce_add) tma_reduce_add_2d(mC, sb, tl.mb * kBM + 32 * wq, n0 + c0);
+            else tma_store_2d(mC, sb, tl.mb * kBM + 32 * wq, n0 + c0);
+          }
+          if (lane == 0) bulk_commit();
+          ++nstore;
+          buf ^= 1;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
       } else {
         const CUtensorMap* mC = &g.tmC[tl.prob];
         const bool box_live = tl.mb * kBM + 32 * wq < P.M;
@@ -422,6 +487,8 @@ cudaError_t launch(const GemmArgs& a, int num_sms, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   int grid = a.total_tiles < num_sms ? a.total_tiles : num_sms;
   if (grid < 1) return cudaSuccess;
+  e = cudaMemsetAsync(a.tile_counter, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
   k<<<grid, kThreads, C::SMEM, s>>>(a);
   return cudaGetLastError();
 }

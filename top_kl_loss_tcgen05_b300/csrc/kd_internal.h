@@ -13,7 +13,7 @@ namespace kd {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kBNLogits = 256;  // forward / recompute: N tile over the vocabulary
-constexpr int kBNGrad = 192;    // dH / dW: N tile over the hidden size d
+constexpr int kBNGrad = 256;    // dH^T / dW: N tile
 
 // One GEMM problem of a launch: C[M, N] = sum_k A[m, k] B[n, k].
 struct Problem {
@@ -23,6 +23,7 @@ struct Problem {
   int tile_begin;   // first global tile index of this problem
   int n_fastest;    // tile order: 1 = consecutive tiles walk N, 0 = walk M
   int reduce_add;   // fp32 epilogue: 1 = TMA reduce-add into C, 0 = store
+  int c_trans;      // fp32 epilogue: 1 = write C^T (TMEM lanes are C's columns)
 };
 
 // Kernel parameters (passed as __grid_constant__; tensor maps live in param space).
@@ -33,6 +34,7 @@ struct GemmArgs {
   Problem pr[2];
   int nprob;
   int total_tiles;
+  int* tile_counter;      // dynamic tile scheduler (zeroed before each launch)
   // fused-epilogue data (chunk-local rows)
   int rows;               // rows of this chunk
   int row_stride;         // stride of the [S][chunk] partial arrays (= chunk)
@@ -66,6 +68,7 @@ cudaError_t launch_merge(const float* part_m, const float* part_s, int S, int ro
                          float* lse_out, float* loss_rows_out, double* block_sums, cudaStream_t s);
 cudaError_t launch_chunk_reduce(const double* block_sums, int nblocks, double* acc, int first, cudaStream_t s);
 cudaError_t launch_finalize(const double* acc, double inv_T, float* loss, cudaStream_t s);
+cudaError_t launch_transpose(const void* src, int rows, int cols, void* dst, int ld_dst, cudaStream_t s);
 
 // Top-K (kd_topk.cu).
 size_t topk_smem_bytes(int K);

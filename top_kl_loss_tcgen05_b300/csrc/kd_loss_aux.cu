@@ -201,7 +201,32 @@ __global__ void finalize_kernel(const double* acc, double inv_T, float* loss) {
   if (threadIdx.x == 0 && blockIdx.x == 0) *loss = (float)(*acc * inv_T);
 }
 
+// dst[c][r] = src[r][c] for a bf16 [rows, cols] matrix (dst row stride
+// ld_dst): 32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256) transpose_kernel(const uint16_t* __restrict__ src, int rows, int cols,
+                                                        uint16_t* __restrict__ dst, int ld_dst) {
+  __shared__ uint16_t tile[32][34];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int j = ty; j < 32; j += 8) {
+    const int r = r0 + j, c = c0 + tx;
+    if (r < rows && c < cols) tile[j][tx] = src[(size_t)r * cols + c];
+  }
+  __syncthreads();
+  for (int j = ty; j < 32; j += 8) {
+    const int c = c0 + j, r = r0 + tx;
+    if (c < cols && r < rows) dst[(size_t)c * ld_dst + r] = tile[tx][j];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_transpose(const void* src, int rows, int cols, void* dst, int ld_dst, cudaStream_t s) {
+  dim3 grid((cols + 31) / 32, (rows + 31) / 32);
+  transpose_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(src), rows, cols, static_cast<uint16_t*>(dst),
+                                        ld_dst);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prep(const int32_t* ids, const float* logp, int rows, int K, int V, int Kp, int* ids_sorted,
                         float* p_sorted, int* cnt, float* ent, int* status, cudaStream_t s) {

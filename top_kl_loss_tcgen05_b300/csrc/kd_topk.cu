@@ -5,18 +5,22 @@
 // teacher runs once and only its K most probable tokens per position are
 // kept). Selection order: value descending, then id ascending; -0.0 == +0.0.
 //
-// One CTA streams one row from HBM exactly once with 16-byte loads. In that
-// single pass it computes
-//   * the row's log-sum-exp: an online (max, sum of exp) per thread, merged in
-//     a fixed order, so the result is deterministic;
-//   * the top-K candidates: each thread keeps its own best 8 (value, id)
-//     pairs in registers. A vector of 8 logits is skipped with one compare
-//     when its maximum is below the thread's 8th best.
-// The 256 x 8 candidates are sorted in shared memory and the first K taken.
-// This is exact unless some thread dropped an element that ranks at or above
-// the K-th pick. Each thread tracks the best element it dropped, so that case
-// is detected, and then (or when K > 2048) the row is redone by an exact
-// radix selection over the row in global memory (L2-resident by then).
+// Persistent CTAs take rows from an atomic counter. For each row, thread 0
+// streams the row's 16-byte-aligned body from HBM into a 4-stage shared-memory
+// ring with bulk copies (cp.async.bulk, mbarrier completion), so the bytes in
+// flight do not depend on registers. The next row's first chunks are already
+// loading while the current row is being finished. Every byte is read once.
+// From the ring, each thread keeps
+//   * an online (max, sum of exp) of its elements: the row's log-sum-exp,
+//     merged in a fixed order, so the result is deterministic;
+//   * its best 16 (value, id) pairs, sorted, in registers. A vector of 8
+//     logits costs one compare when its maximum is below the thread's 16th best.
+// At the end of a row, a 32-step bisection over the value keys of the 256 x 16
+// candidates finds the K-th largest value. The candidates at or above it are
+// compacted and sorted, and the first K taken. That is exact unless a thread
+// dropped an element ranking at or above the K-th pick: each thread tracks the
+// best element it dropped, so that case is detected. Then (and for K > 1024)
+// the row is redone by an exact radix selection over the row in global memory.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -27,8 +31,12 @@ namespace kd {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kList = 8;                      // per-thread candidate list
-constexpr int kUnion = kThreads * kList;      // 2048 candidates per row
+constexpr int kWarps = kThreads / 32;
+constexpr int kList = 16;        // per-thread candidate list
+constexpr int kStages = 4;       // smem ring depth
+constexpr int kChunk = 16384;    // bytes per ring stage
+constexpr int kSelCap = 1024;    // fast-path compaction buffer (entries)
+constexpr int kFastMaxK = 1024;  // larger K goes to the exact path
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -75,14 +83,28 @@ struct Row<float> {
   }
 };
 
+// Split of a row into scalar head, 16-byte-aligned body and scalar tail.
+template <typename Tin>
+struct RowSplit {
+  int head, nvec, tail0, tail;
+  __device__ RowSplit(const Tin* row, int V) {
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
+    head = (int)(((16u - (addr & 15u)) & 15u) / sizeof(Tin));
+    if (head > V) head = V;
+    nvec = (V - head) / Row<Tin>::kVec;
+    tail0 = head + nvec * Row<Tin>::kVec;
+    tail = V - tail0;
+  }
+};
+
 // Per-thread state of the streaming pass.
 struct Scan {
   float m, s;            // online log-sum-exp: max and sum of exp(x - m)
-  uint64_t L[kList];     // best 8 rank keys, descending; 0 = empty
-  float thr;             // value of L[7] (-inf while the list is not full)
+  uint64_t L[kList];     // best rank keys, descending; 0 = empty
+  float thr;             // value of L[kList-1] (-inf while the list is not full)
   uint64_t drop;         // best rank key this thread dropped (exact)
   float drop_v;          // best value dropped by the one-compare skip
-  __device__ void init() {
+  __device__ __forceinline__ void init() {
     m = -INFINITY; s = 0.f; thr = -INFINITY; drop = 0; drop_v = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kList; ++j) L[j] = 0;
@@ -123,7 +145,10 @@ struct Scan {
       drop_v = fmaxf(drop_v, vmax);
     } else {
 #pragma unroll
-      for (int j = 0; j < N; ++j) offer(x[j], id0 + j);
+      for (int j = 0; j < N; ++j) {
+        if (x[j] >= thr) offer(x[j], id0 + j);
+        else drop_v = fmaxf(drop_v, x[j]);
+      }
     }
   }
   __device__ __forceinline__ void one(float x, uint32_t id) {
@@ -174,36 +199,63 @@ __device__ int block_excl_scan(int v, int* sm_warp, int* total) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int acc = 0;
-    for (int i = 0; i < kThreads / 32; ++i) { const int t = sm_warp[i]; sm_warp[i] = acc; acc += t; }
-    sm_warp[kThreads / 32] = acc;
+    for (int i = 0; i < kWarps; ++i) { const int t = sm_warp[i]; sm_warp[i] = acc; acc += t; }
+    sm_warp[kWarps] = acc;
   }
   __syncthreads();
   const int r = sm_warp[w] + inc - v;
-  *total = sm_warp[kThreads / 32];
+  *total = sm_warp[kWarps];
   __syncthreads();
   return r;
 }
 
+// Loads the 8 (bf16) or 4 (fp32) elements of body vector i of a row.
 template <typename Tin>
-__device__ __forceinline__ float load_elem(const Tin* row, int64_t j) {
-  return Row<Tin>::cvt(row[j]);
+__device__ __forceinline__ void load_vec(const Tin* row, const RowSplit<Tin>& rs, int i,
+                                         float (&x)[Row<Tin>::kVec]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + rs.head) + i);
+  Row<Tin>::unpack(u, x);
 }
 
 // Exact top-K by radix selection on the order keys, reading the row from
-// global memory. Writes the K rank keys, sorted descending, to cand[0..K).
+// global memory (it is usually still in L2). Writes the K rank keys, sorted
+// descending, to cand[0..K) (cand holds n_pow2 >= K entries).
 template <typename Tin>
 __device__ void exact_select(const Tin* row, int V, int K, uint64_t* cand, int n_pow2, uint32_t* hist,
                              int* sm_scan, int* sm_misc) {
-  const int tid = threadIdx.x;
+  constexpr int VEC = Row<Tin>::kVec;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const RowSplit<Tin> rs(row, V);
   uint32_t prefix = 0, pmask = 0;
   int krem = K;
   const int last_shift = sizeof(Tin) == 2 ? 16 : 0;
   for (int shift = 24; shift >= last_shift; shift -= 8) {
     for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
     __syncthreads();
-    for (int j = tid; j < V; j += kThreads) {
-      const uint32_t k = okey(load_elem(row, j));
+    // scalar head and tail
+    for (int j = tid; j < rs.head; j += kThreads) {
+      const uint32_t k = okey(Row<Tin>::cvt(row[j]));
       if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+    }
+    for (int j = tid; j < rs.tail; j += kThreads) {
+      const uint32_t k = okey(Row<Tin>::cvt(row[rs.tail0 + j]));
+      if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+    }
+    // body: warp-uniform trip count, warp-aggregated increments
+    for (int b = warp * 32; b < rs.nvec; b += kThreads) {
+      const int i = b + lane;
+      float x[VEC];
+      if (i < rs.nvec) load_vec(row, rs, i, x);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        uint32_t dig = 256u;
+        if (i < rs.nvec) {
+          const uint32_t k = okey(x[j]);
+          if ((k & pmask) == prefix) dig = (k >> shift) & 255u;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, dig);
+        if (dig < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[dig], (uint32_t)__popc(peers));
+      }
     }
     __syncthreads();
     if (tid == 0) {
@@ -232,155 +284,300 @@ __device__ void exact_select(const Tin* row, int V, int K, uint64_t* cand, int n
   for (int i = tid; i < n_pow2; i += kThreads) cand[i] = 0;
   if (tid == 0) sm_misc[2] = 0;
   __syncthreads();
-  for (int j = tid; j < V; j += kThreads) {
-    const float x = load_elem(row, j);
-    if (okey(x) > kth) {
-      const int slot = atomicAdd(&sm_misc[2], 1);
-      cand[slot] = rkey(x, (uint32_t)j);
-    }
+  // elements strictly above the K-th value (order does not matter here)
+  for (int j = tid; j < rs.head; j += kThreads) {
+    const float x = Row<Tin>::cvt(row[j]);
+    if (okey(x) > kth) cand[atomicAdd(&sm_misc[2], 1)] = rkey(x, (uint32_t)j);
+  }
+  for (int j = tid; j < rs.tail; j += kThreads) {
+    const float x = Row<Tin>::cvt(row[rs.tail0 + j]);
+    if (okey(x) > kth) cand[atomicAdd(&sm_misc[2], 1)] = rkey(x, (uint32_t)(rs.tail0 + j));
+  }
+  for (int i = tid; i < rs.nvec; i += kThreads) {
+    float x[VEC];
+    load_vec(row, rs, i, x);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j)
+      if (okey(x[j]) > kth) cand[atomicAdd(&sm_misc[2], 1)] = rkey(x[j], (uint32_t)(rs.head + i * VEC + j));
   }
   __syncthreads();
-  // Equal elements in id order: 8 consecutive elements per thread per tile.
+  // elements equal to the K-th value, in id order: head, body vectors, tail
   int taken = 0;
-  for (int base = 0; base < V && taken < need_eq; base += kThreads * 8) {
-    const int j0 = base + tid * 8;
+  {
     int c = 0;
-    for (int q = 0; q < 8; ++q) {
-      const int j = j0 + q;
-      if (j < V && okey(load_elem(row, j)) == kth) ++c;
+    float xh = 0.f;
+    if (tid < rs.head) { xh = Row<Tin>::cvt(row[tid]); c = okey(xh) == kth; }
+    int tot;
+    const int r = block_excl_scan(c, sm_scan, &tot);
+    if (c && taken + r < need_eq) cand[n_gt + taken + r] = rkey(xh, (uint32_t)tid);
+    taken += tot;
+  }
+  for (int base = 0; base < rs.nvec && taken < need_eq; base += kThreads) {
+    const int i = base + tid;
+    float x[VEC];
+    int c = 0;
+    if (i < rs.nvec) {
+      load_vec(row, rs, i, x);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) c += okey(x[j]) == kth;
     }
     int tot;
     int r = block_excl_scan(c, sm_scan, &tot);
-    for (int q = 0; q < 8 && c > 0; ++q) {
-      const int j = j0 + q;
-      if (j < V) {
-        const float x = load_elem(row, j);
-        if (okey(x) == kth) {
-          if (taken + r < need_eq) cand[n_gt + taken + r] = rkey(x, (uint32_t)j);
+    if (c) {
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        if (okey(x[j]) == kth) {
+          if (taken + r < need_eq) cand[n_gt + taken + r] = rkey(x[j], (uint32_t)(rs.head + i * VEC + j));
           ++r;
         }
       }
     }
     taken += tot;  // block-uniform
   }
+  if (taken < need_eq) {
+    int c = 0;
+    float xt = 0.f;
+    if (tid < rs.tail) { xt = Row<Tin>::cvt(row[rs.tail0 + tid]); c = okey(xt) == kth; }
+    int tot;
+    const int r = block_excl_scan(c, sm_scan, &tot);
+    if (c && taken + r < need_eq) cand[n_gt + taken + r] = rkey(xt, (uint32_t)(rs.tail0 + tid));
+  }
   __syncthreads();
   bitonic_desc(cand, n_pow2);
 }
 
+struct Ring {
+  uint64_t full[kStages];
+  int row[kStages];
+  int chunk[kStages];
+  int bytes[kStages];
+  int last[kStages];
+};
+
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const Tin* __restrict__ logits, int64_t T, int V,
-                                                        int64_t ld, int K, int cand_n, int force_exact,
+                                                        int64_t ld, int K, int sel_n, int force_exact,
                                                         int32_t* __restrict__ ids, float* __restrict__ logp,
                                                         int* __restrict__ ws_words) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* ring = smem_raw;  // kStages x kChunk
+  uint64_t* sel = reinterpret_cast<uint64_t*>(smem_raw + kStages * kChunk);
+  __shared__ Ring R;
   __shared__ uint32_t hist[256];
-  __shared__ int sm_scan[kThreads / 32 + 1];
+  __shared__ int sm_scan[kWarps + 1];
   __shared__ int sm_misc[4];
-  __shared__ float sm_m[kThreads / 32], sm_s[kThreads / 32];
+  __shared__ int sm_cnt[2][kWarps];
+  __shared__ float sm_m[kWarps], sm_s[kWarps];
   __shared__ float sm_lse;
-  __shared__ int sm_ok;
+  __shared__ int sm_abort;
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int VEC = Row<Tin>::kVec;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* status = ws_words;
+  int* row_counter = ws_words + 2;
 
-  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-    const Tin* row = logits + t * ld;
-    Scan st;
-    st.init();
-    // Head elements up to the first 16-byte boundary, then 16-byte vectors,
-    // then the tail.
-    const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
-    int head = (int)(((16u - (addr & 15u)) & 15u) / sizeof(Tin));
-    if (head > V) head = V;
-    const int nvec = (V - head) / VEC;
-    const int tail0 = head + nvec * VEC;
-    if (tid < head) st.one(Row<Tin>::cvt(row[tid]), (uint32_t)tid);
-    if (tid < V - tail0) st.one(Row<Tin>::cvt(row[tail0 + tid]), (uint32_t)(tail0 + tid));
-    const uint4* vrow = reinterpret_cast<const uint4*>(row + head);
-    int i = tid;
-    for (; i + 3 * kThreads < nvec; i += 4 * kThreads) {
-      uint4 u[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) u[q] = __ldcs(vrow + i + q * kThreads);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float x[VEC];
-        Row<Tin>::unpack(u[q], x);
-        st.vec(x, (uint32_t)(head + (i + q * kThreads) * VEC));
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&R.full[s], 1);
+    sm_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // Producer state (thread 0 only).
+  int p_row = -1, p_chunk = 0, p_nch = 0;
+  bool p_done = false;
+  int issued_use[kStages];
+  for (int s = 0; s < kStages; ++s) issued_use[s] = -1;
+  auto produce = [&](int s, int use) {
+    if (p_row >= 0 && p_chunk >= p_nch) p_row = -1;
+    if (p_row < 0 && !p_done) {
+      const int r = atomicAdd(row_counter, 1);
+      if (r < T) {
+        p_row = r;
+        p_chunk = 0;
+        const RowSplit<Tin> rs(logits + (int64_t)r * ld, V);
+        const int body = rs.nvec * 16;
+        p_nch = body > 0 ? (body + kChunk - 1) / kChunk : 1;
+      } else {
+        p_done = true;
       }
     }
-    for (; i < nvec; i += kThreads) {
-      const uint4 u = __ldcs(vrow + i);
-      float x[VEC];
-      Row<Tin>::unpack(u, x);
-      st.vec(x, (uint32_t)(head + i * VEC));
+    if (p_row < 0) {
+      R.row[s] = -1;
+      R.bytes[s] = 0;
+      mbar_arrive(&R.full[s]);
+      return;
     }
+    const Tin* rp = logits + (int64_t)p_row * ld;
+    const RowSplit<Tin> rs(rp, V);
+    const int body = rs.nvec * 16;
+    const int off = p_chunk * kChunk;
+    const int bytes = body - off < kChunk ? body - off : kChunk;
+    R.row[s] = p_row;
+    R.chunk[s] = p_chunk;
+    R.bytes[s] = bytes > 0 ? bytes : 0;
+    R.last[s] = (p_chunk == p_nch - 1);
+    if (bytes > 0) {
+      mbar_arrive_expect_tx(&R.full[s], (uint32_t)bytes);
+      bulk_load(smem_u32(ring + s * kChunk), reinterpret_cast<const unsigned char*>(rp + rs.head) + off,
+                (uint32_t)bytes, &R.full[s]);
+      issued_use[s] = use;
+    } else {
+      mbar_arrive(&R.full[s]);
+    }
+    ++p_chunk;
+  };
+  if (tid == 0)
+    for (int s = 0; s < kStages; ++s) produce(s, 0);
 
-    // Row log-sum-exp, merged in a fixed order.
-    float m = st.m, s = st.s;
+  Scan st;
+  st.init();
+  for (int it = 0;; ++it) {
+    const int s = it % kStages;
+    const int use = it / kStages;
+    const bool ok_wait = mbar_wait(&R.full[s], (uint32_t)(use & 1), &sm_abort);
+    const int row = R.row[s];
+    if (__syncthreads_or(!ok_wait)) {
+      if (tid == 0) {
+        set_status(status, ST_TIMEOUT);
+        // drain: wait (bounded) for every bulk copy this CTA issued
+        for (int q = 0; q < kStages; ++q) {
+          if (issued_use[q] < 0) continue;
+          const uint32_t a = smem_u32(&R.full[q]);
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(a, (uint32_t)(issued_use[q] & 1))) {
+            if (globaltimer() - t0 > kWaitLimitNs) break;
+          }
+        }
+      }
+      break;
+    }
+    if (row < 0) break;  // uniform: every thread read the same slot
+    const Tin* rp = logits + (int64_t)row * ld;
+    const RowSplit<Tin> rs(rp, V);
+    const int chunk = R.chunk[s];
+    const int nv = R.bytes[s] / 16;
+    const bool last = R.last[s] != 0;
+    if (chunk == 0) {
+      st.init();
+      if (tid < rs.head) st.one(Row<Tin>::cvt(rp[tid]), (uint32_t)tid);
+      if (tid < rs.tail) st.one(Row<Tin>::cvt(rp[rs.tail0 + tid]), (uint32_t)(rs.tail0 + tid));
+    }
+    {
+      const uint4* vs = reinterpret_cast<const uint4*>(ring + s * kChunk);
+      const uint32_t id0 = (uint32_t)(rs.head + chunk * (kChunk / (int)sizeof(Tin)));
+      for (int i = tid; i < nv; i += kThreads) {
+        const uint4 u = vs[i];
+        float x[VEC];
+        Row<Tin>::unpack(u, x);
+        st.vec(x, id0 + (uint32_t)(i * VEC));
+      }
+    }
+    __syncthreads();  // stage s consumed by every thread
+    if (tid == 0) produce(s, use + 1);
+    if (!last) continue;
+
+    // ---------------------------------------------------------- finish the row
+    float m = st.m, sum = st.s;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      lse_merge(m, s, m2, s2);
+      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+      lse_merge(m, sum, m2, s2);
     }
-    if (lane == 0) { sm_m[warp] = m; sm_s[warp] = s; }
-
-    // Candidate union.
-    bool exact = force_exact || K > kUnion;
-    if (!exact) {
-#pragma unroll
-      for (int j = 0; j < kList; ++j) cand[tid * kList + j] = st.L[j];
-    }
+    if (lane == 0) { sm_m[warp] = m; sm_s[warp] = sum; }
+    if (tid == 0) sm_misc[3] = 0;
     __syncthreads();
     if (tid == 0) {
       float M = sm_m[0], S = sm_s[0];
-      for (int w = 1; w < kThreads / 32; ++w) lse_merge(M, S, sm_m[w], sm_s[w]);
+      for (int w = 1; w < kWarps; ++w) lse_merge(M, S, sm_m[w], sm_s[w]);
       sm_lse = M + logf(S);
     }
+
+    bool exact = force_exact || K > kFastMaxK;
     if (!exact) {
-      bitonic_desc(cand, kUnion);
-      const uint64_t eK = cand[K - 1];
-      const float eKv = okey_to_float((uint32_t)(eK >> 32));
-      const bool ok = eK != 0 && st.drop < eK && st.drop_v < eKv;
-      exact = !__syncthreads_and(ok);
+      // K-th largest value key of the union, bit by bit.
+      uint32_t kth = 0;
+      for (int b = 31; b >= 0; --b) {
+        const uint32_t cand = kth | (1u << b);
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < kList; ++j) c += ((uint32_t)(st.L[j] >> 32) >= cand) ? 1 : 0;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (lane == 0) sm_cnt[b & 1][warp] = c;
+        __syncthreads();
+        int tot = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) tot += sm_cnt[b & 1][w];
+        if (tot >= K) kth = cand;
+      }
+      // Compact the candidates with value key >= kth (a prefix of each list).
+      int my = 0;
+#pragma unroll
+      for (int j = 0; j < kList; ++j) my += ((uint32_t)(st.L[j] >> 32) >= kth) ? 1 : 0;
+      int inc = my;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      int base = 0;
+      if (lane == 31) base = atomicAdd(&sm_misc[3], inc);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      const int off = base + inc - my;
+#pragma unroll
+      for (int j = 0; j < kList; ++j)
+        if (j < my && off + j < kSelCap) sel[off + j] = st.L[j];
+      __syncthreads();
+      const int nsel = sm_misc[3];
+      if (kth == 0 || nsel > kSelCap || nsel < K) {
+        exact = true;
+      } else {
+        int n2 = 1;
+        while (n2 < nsel) n2 <<= 1;
+        for (int i = nsel + tid; i < n2; i += kThreads) sel[i] = 0;
+        __syncthreads();
+        bitonic_desc(sel, n2);
+        const uint64_t eK = sel[K - 1];
+        const float eKv = okey_to_float((uint32_t)(eK >> 32));
+        const bool ok = eK != 0 && st.drop < eK && st.drop_v < eKv;
+        exact = !__syncthreads_and(ok);
+      }
     }
     if (exact) {
-      if (tid == 0 && !force_exact && ws_words) atomicAdd(&ws_words[1], 1);
+      if (tid == 0 && !force_exact) atomicAdd(&ws_words[1], 1);
       __syncthreads();
-      exact_select<Tin>(row, V, K, cand, cand_n, hist, sm_scan, sm_misc);
+      exact_select<Tin>(rp, V, K, sel, sel_n, hist, sm_scan, sm_misc);
     }
     __syncthreads();
     const float lse = sm_lse;
     for (int k = tid; k < K; k += kThreads) {
-      const uint64_t c = cand[k];
-      ids[t * K + k] = (int32_t)(0xFFFFFFFFu - (uint32_t)c);
-      logp[t * K + k] = okey_to_float((uint32_t)(c >> 32)) - lse;
+      const uint64_t c = sel[k];
+      ids[(int64_t)row * K + k] = (int32_t)(0xFFFFFFFFu - (uint32_t)c);
+      logp[(int64_t)row * K + k] = okey_to_float((uint32_t)(c >> 32)) - lse;
     }
     __syncthreads();
   }
-  (void)sm_ok;
+}
+
+int sel_entries(int K) {
+  int n = 1;
+  while (n < K) n <<= 1;
+  return n < kSelCap ? kSelCap : n;
 }
 
 }  // namespace
 
-size_t topk_smem_bytes(int K) {
-  int n = 1;
-  while (n < K) n <<= 1;
-  if (n < kUnion) n = kUnion;
-  return (size_t)n * sizeof(uint64_t);
-}
+size_t topk_smem_bytes(int K) { return (size_t)kStages * kChunk + (size_t)sel_entries(K) * sizeof(uint64_t); }
 
 cudaError_t launch_topk(const void* logits, int dtype, int64_t T, int64_t V, int64_t ld, int K,
                         int32_t* ids, float* logp, int* ws_words, int force_exact, int num_sms,
                         cudaStream_t stream) {
-  int n = 1;
-  while (n < K) n <<= 1;
-  if (n < kUnion) n = kUnion;
-  const size_t smem = (size_t)n * sizeof(uint64_t);
+  const int n = sel_entries(K);
+  const size_t smem = topk_smem_bytes(K);
   int blocks_per_sm = 0;
-  cudaError_t e;
+  cudaError_t e = cudaMemsetAsync(ws_words + 2, 0, sizeof(int), stream);  // row counter
+  if (e != cudaSuccess) return e;
   if (dtype == 0) {
     e = cudaFuncSetAttribute(topk_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
