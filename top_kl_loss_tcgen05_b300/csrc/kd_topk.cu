@@ -5,22 +5,23 @@
 // teacher runs once and only its K most probable tokens per position are
 // kept). Selection order: value descending, then id ascending; -0.0 == +0.0.
 //
-// Persistent CTAs take rows from an atomic counter. For each row, thread 0
-// streams the row's 16-byte-aligned body from HBM into a 4-stage shared-memory
-// ring with bulk copies (cp.async.bulk, mbarrier completion), so the bytes in
-// flight do not depend on registers. The next row's first chunks are already
-// loading while the current row is being finished. Every byte is read once.
-// From the ring, each thread keeps
-//   * an online (max, sum of exp) of its elements: the row's log-sum-exp,
-//     merged in a fixed order, so the result is deterministic;
-//   * its best 16 (value, id) pairs, sorted, in registers. A vector of 8
-//     logits costs one compare when its maximum is below the thread's 16th best.
-// At the end of a row, a 32-step bisection over the value keys of the 256 x 16
-// candidates finds the K-th largest value. The candidates at or above it are
-// compacted and sorted, and the first K taken. That is exact unless a thread
-// dropped an element ranking at or above the K-th pick: each thread tracks the
-// best element it dropped, so that case is detected. Then (and for K > 1024)
-// the row is redone by an exact radix selection over the row in global memory.
+// Persistent CTAs (two per SM) take rows from an atomic counter; per row:
+//   pass 1  stream the row from HBM with 16-byte loads (8 per thread in
+//           flight). Each thread keeps an online (max, sum of exp) of its
+//           elements. That is the log-sum-exp, merged in a fixed order
+//           (deterministic), and its max is a statistic for the selection.
+//   tau     the K-th largest of the 256 per-thread maxima, found by a
+//           bisection over the value keys (one __syncthreads_count per bit).
+//           The maxima are K distinct elements >= tau, so tau is a lower
+//           bound of the row's K-th largest value. On the pages' workload only
+//           about 200 elements of a 201088-wide row are >= tau.
+//   pass 2  re-read the row (now in L2, loads marked evict-first) and append
+//           every element >= tau to a shared buffer. It holds every top-K
+//           element, ties included.
+//   select  sort the buffer by (value desc, id asc); its first K entries are
+//           the cache row.
+// If the buffer overflows (massive ties) or K > 1024, the row is redone by an
+// exact radix selection over the row in global memory.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -32,11 +33,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kList = 16;        // per-thread candidate list
-constexpr int kStages = 4;       // smem ring depth
-constexpr int kChunk = 16384;    // bytes per ring stage
-constexpr int kSelCap = 1024;    // fast-path compaction buffer (entries)
+constexpr int kCandCap = 2048;   // candidate buffer entries (fast path)
 constexpr int kFastMaxK = 1024;  // larger K goes to the exact path
+constexpr int kBatch = 8;        // 16-byte loads per thread in flight in pass 1
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -97,64 +96,26 @@ struct RowSplit {
   }
 };
 
-// Per-thread state of the streaming pass.
-struct Scan {
-  float m, s;            // online log-sum-exp: max and sum of exp(x - m)
-  uint64_t L[kList];     // best rank keys, descending; 0 = empty
-  float thr;             // value of L[kList-1] (-inf while the list is not full)
-  uint64_t drop;         // best rank key this thread dropped (exact)
-  float drop_v;          // best value dropped by the one-compare skip
-  __device__ __forceinline__ void init() {
-    m = -INFINITY; s = 0.f; thr = -INFINITY; drop = 0; drop_v = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kList; ++j) L[j] = 0;
-  }
-  __device__ __forceinline__ void lse_max(float vmax) {
+// Per-thread online log-sum-exp.
+struct Lse {
+  float m, s;  // max and sum of exp(x - m)
+  __device__ __forceinline__ void init() { m = -INFINITY; s = 0.f; }
+  __device__ __forceinline__ void max_to(float vmax) {
     if (vmax > m) {
       s *= ex2((m - vmax) * kLog2e);
       m = vmax;
     }
   }
-  __device__ __forceinline__ void offer(float x, uint32_t id) {
-    const uint64_t k = rkey(x, id);
-    if (k > L[kList - 1]) {
-      if (L[kList - 1] > drop) drop = L[kList - 1];
-      L[kList - 1] = k;
-#pragma unroll
-      for (int j = kList - 1; j > 0; --j) {
-        const uint64_t a = L[j - 1], b = L[j];
-        const bool sw = b > a;
-        L[j - 1] = sw ? b : a;
-        L[j] = sw ? a : b;
-      }
-      thr = L[kList - 1] ? okey_to_float((uint32_t)(L[kList - 1] >> 32)) : -INFINITY;
-    } else if (k > drop) {
-      drop = k;
-    }
-  }
   template <int N>
-  __device__ __forceinline__ void vec(const float (&x)[N], uint32_t id0) {
-    float vmax = x[0];
-#pragma unroll
-    for (int j = 1; j < N; ++j) vmax = fmaxf(vmax, x[j]);
-    lse_max(vmax);
+  __device__ __forceinline__ void add(const float (&x)[N], float vmax) {
+    max_to(vmax);
     const float mb = -m * kLog2e;
 #pragma unroll
     for (int j = 0; j < N; ++j) s += ex2(fmaf(x[j], kLog2e, mb));
-    if (vmax < thr) {
-      drop_v = fmaxf(drop_v, vmax);
-    } else {
-#pragma unroll
-      for (int j = 0; j < N; ++j) {
-        if (x[j] >= thr) offer(x[j], id0 + j);
-        else drop_v = fmaxf(drop_v, x[j]);
-      }
-    }
   }
-  __device__ __forceinline__ void one(float x, uint32_t id) {
-    lse_max(x);
+  __device__ __forceinline__ void one(float x) {
+    max_to(x);
     s += ex2((x - m) * kLog2e);
-    offer(x, id);
   }
 };
 
@@ -346,138 +307,62 @@ __device__ void exact_select(const Tin* row, int V, int K, uint64_t* cand, int n
   bitonic_desc(cand, n_pow2);
 }
 
-struct Ring {
-  uint64_t full[kStages];
-  int row[kStages];
-  int chunk[kStages];
-  int bytes[kStages];
-  int last[kStages];
-};
-
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads) topk_kernel(const Tin* __restrict__ logits, int64_t T, int V,
-                                                        int64_t ld, int K, int sel_n, int force_exact,
-                                                        int32_t* __restrict__ ids, float* __restrict__ logp,
-                                                        int* __restrict__ ws_words) {
+__global__ void __launch_bounds__(kThreads, 2) topk_kernel(const Tin* __restrict__ logits, int64_t T, int V,
+                                                           int64_t ld, int K, int force_exact,
+                                                           int32_t* __restrict__ ids, float* __restrict__ logp,
+                                                           int* __restrict__ ws_words) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  unsigned char* ring = smem_raw;  // kStages x kChunk
-  uint64_t* sel = reinterpret_cast<uint64_t*>(smem_raw + kStages * kChunk);
-  __shared__ Ring R;
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);  // sel_entries(K) entries
   __shared__ uint32_t hist[256];
   __shared__ int sm_scan[kWarps + 1];
   __shared__ int sm_misc[4];
-  __shared__ int sm_cnt[2][kWarps];
   __shared__ float sm_m[kWarps], sm_s[kWarps];
   __shared__ float sm_lse;
-  __shared__ int sm_abort;
+  __shared__ int sm_n;
+  __shared__ int sm_next;
 
   constexpr int VEC = Row<Tin>::kVec;
+  constexpr int kLoBits = sizeof(Tin) == 2 ? 16 : 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int* status = ws_words;
   int* row_counter = ws_words + 2;
+  const bool fast = !force_exact && K <= kFastMaxK;
 
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&R.full[s], 1);
-    sm_abort = 0;
-    fence_mbar_init();
-  }
+  if (tid == 0) sm_next = atomicAdd(row_counter, 1);
   __syncthreads();
-
-  // Producer state (thread 0 only).
-  int p_row = -1, p_chunk = 0, p_nch = 0;
-  bool p_done = false;
-  int issued_use[kStages];
-  for (int s = 0; s < kStages; ++s) issued_use[s] = -1;
-  auto produce = [&](int s, int use) {
-    if (p_row >= 0 && p_chunk >= p_nch) p_row = -1;
-    if (p_row < 0 && !p_done) {
-      const int r = atomicAdd(row_counter, 1);
-      if (r < T) {
-        p_row = r;
-        p_chunk = 0;
-        const RowSplit<Tin> rs(logits + (int64_t)r * ld, V);
-        const int body = rs.nvec * 16;
-        p_nch = body > 0 ? (body + kChunk - 1) / kChunk : 1;
-      } else {
-        p_done = true;
-      }
-    }
-    if (p_row < 0) {
-      R.row[s] = -1;
-      R.bytes[s] = 0;
-      mbar_arrive(&R.full[s]);
-      return;
-    }
-    const Tin* rp = logits + (int64_t)p_row * ld;
-    const RowSplit<Tin> rs(rp, V);
-    const int body = rs.nvec * 16;
-    const int off = p_chunk * kChunk;
-    const int bytes = body - off < kChunk ? body - off : kChunk;
-    R.row[s] = p_row;
-    R.chunk[s] = p_chunk;
-    R.bytes[s] = bytes > 0 ? bytes : 0;
-    R.last[s] = (p_chunk == p_nch - 1);
-    if (bytes > 0) {
-      mbar_arrive_expect_tx(&R.full[s], (uint32_t)bytes);
-      bulk_load(smem_u32(ring + s * kChunk), reinterpret_cast<const unsigned char*>(rp + rs.head) + off,
-                (uint32_t)bytes, &R.full[s]);
-      issued_use[s] = use;
-    } else {
-      mbar_arrive(&R.full[s]);
-    }
-    ++p_chunk;
-  };
-  if (tid == 0)
-    for (int s = 0; s < kStages; ++s) produce(s, 0);
-
-  Scan st;
-  st.init();
-  for (int it = 0;; ++it) {
-    const int s = it % kStages;
-    const int use = it / kStages;
-    const bool ok_wait = mbar_wait(&R.full[s], (uint32_t)(use & 1), &sm_abort);
-    const int row = R.row[s];
-    if (__syncthreads_or(!ok_wait)) {
-      if (tid == 0) {
-        set_status(status, ST_TIMEOUT);
-        // drain: wait (bounded) for every bulk copy this CTA issued
-        for (int q = 0; q < kStages; ++q) {
-          if (issued_use[q] < 0) continue;
-          const uint32_t a = smem_u32(&R.full[q]);
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(a, (uint32_t)(issued_use[q] & 1))) {
-            if (globaltimer() - t0 > kWaitLimitNs) break;
-          }
-        }
-      }
-      break;
-    }
-    if (row < 0) break;  // uniform: every thread read the same slot
+  int row = sm_next;
+  __syncthreads();
+  while (row < T) {
+    if (tid == 0) sm_next = atomicAdd(row_counter, 1);  // read after this row's barriers
     const Tin* rp = logits + (int64_t)row * ld;
     const RowSplit<Tin> rs(rp, V);
-    const int chunk = R.chunk[s];
-    const int nv = R.bytes[s] / 16;
-    const bool last = R.last[s] != 0;
-    if (chunk == 0) {
-      st.init();
-      if (tid < rs.head) st.one(Row<Tin>::cvt(rp[tid]), (uint32_t)tid);
-      if (tid < rs.tail) st.one(Row<Tin>::cvt(rp[rs.tail0 + tid]), (uint32_t)(rs.tail0 + tid));
-    }
-    {
-      const uint4* vs = reinterpret_cast<const uint4*>(ring + s * kChunk);
-      const uint32_t id0 = (uint32_t)(rs.head + chunk * (kChunk / (int)sizeof(Tin)));
-      for (int i = tid; i < nv; i += kThreads) {
-        const uint4 u = vs[i];
-        float x[VEC];
-        Row<Tin>::unpack(u, x);
-        st.vec(x, id0 + (uint32_t)(i * VEC));
+    const uint4* vr = reinterpret_cast<const uint4*>(rp + rs.head);
+    const int nv = rs.nvec;
+
+    // ---- pass 1: log-sum-exp and per-thread maximum
+    Lse st;
+    st.init();
+    if (tid < rs.head) st.one(Row<Tin>::cvt(rp[tid]));
+    if (tid < rs.tail) st.one(Row<Tin>::cvt(rp[rs.tail0 + tid]));
+    for (int i0 = tid; i0 < nv; i0 += kBatch * kThreads) {
+      uint4 u[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int i = i0 + q * kThreads;
+        u[q] = i < nv ? __ldg(vr + i) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (i0 + q * kThreads < nv) {
+          float x[VEC];
+          Row<Tin>::unpack(u[q], x);
+          float vmax = x[0];
+#pragma unroll
+          for (int j = 1; j < VEC; ++j) vmax = fmaxf(vmax, x[j]);
+          st.add(x, vmax);
+        }
       }
     }
-    __syncthreads();  // stage s consumed by every thread
-    if (tid == 0) produce(s, use + 1);
-    if (!last) continue;
-
-    // ---------------------------------------------------------- finish the row
     float m = st.m, sum = st.s;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -486,94 +371,116 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const Tin* __restrict__ 
       lse_merge(m, sum, m2, s2);
     }
     if (lane == 0) { sm_m[warp] = m; sm_s[warp] = sum; }
-    if (tid == 0) sm_misc[3] = 0;
+    if (tid == 0) sm_n = 0;
     __syncthreads();
     if (tid == 0) {
-      float M = sm_m[0], S = sm_s[0];
-      for (int w = 1; w < kWarps; ++w) lse_merge(M, S, sm_m[w], sm_s[w]);
-      sm_lse = M + logf(S);
+      float M = sm_m[0], Sm = sm_s[0];
+      for (int w = 1; w < kWarps; ++w) lse_merge(M, Sm, sm_m[w], sm_s[w]);
+      sm_lse = M + logf(Sm);
     }
 
-    bool exact = force_exact || K > kFastMaxK;
-    if (!exact) {
-      // K-th largest value key of the union, bit by bit.
+    bool exact = !fast;
+    if (fast) {
+      // ---- tau: K-th largest of the per-thread maxima (key 0 = no element)
+      const uint32_t mykey = st.m == -INFINITY ? 0u : okey(st.m);
       uint32_t kth = 0;
-      for (int b = 31; b >= 0; --b) {
-        const uint32_t cand = kth | (1u << b);
-        int c = 0;
-#pragma unroll
-        for (int j = 0; j < kList; ++j) c += ((uint32_t)(st.L[j] >> 32) >= cand) ? 1 : 0;
-        c = __reduce_add_sync(0xffffffffu, c);
-        if (lane == 0) sm_cnt[b & 1][warp] = c;
-        __syncthreads();
-        int tot = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) tot += sm_cnt[b & 1][w];
-        if (tot >= K) kth = cand;
+      for (int b = 31; b >= kLoBits; --b) {
+        const uint32_t c = kth | (1u << b);
+        if (__syncthreads_count(mykey >= c) >= K) kth = c;
       }
-      // Compact the candidates with value key >= kth (a prefix of each list).
-      int my = 0;
-#pragma unroll
-      for (int j = 0; j < kList; ++j) my += ((uint32_t)(st.L[j] >> 32) >= kth) ? 1 : 0;
-      int inc = my;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
+      if (kLoBits && kth) kth |= (kth & 0x80000000u) ? 0u : ((1u << kLoBits) - 1u);
+      const float tau = kth ? okey_to_float(kth) : -INFINITY;
+
+      // ---- pass 2: every element >= tau into the candidate buffer
+      if (tid < rs.head) {
+        const float x = Row<Tin>::cvt(rp[tid]);
+        if (x >= tau) {
+          const int p = atomicAdd(&sm_n, 1);
+          if (p < kCandCap) cand[p] = rkey(x, (uint32_t)tid);
+        }
       }
-      int base = 0;
-      if (lane == 31) base = atomicAdd(&sm_misc[3], inc);
-      base = __shfl_sync(0xffffffffu, base, 31);
-      const int off = base + inc - my;
+      if (tid < rs.tail) {
+        const float x = Row<Tin>::cvt(rp[rs.tail0 + tid]);
+        if (x >= tau) {
+          const int p = atomicAdd(&sm_n, 1);
+          if (p < kCandCap) cand[p] = rkey(x, (uint32_t)(rs.tail0 + tid));
+        }
+      }
+      for (int i0 = tid; i0 < nv; i0 += kBatch * kThreads) {
+        uint4 u[kBatch];
 #pragma unroll
-      for (int j = 0; j < kList; ++j)
-        if (j < my && off + j < kSelCap) sel[off + j] = st.L[j];
+        for (int q = 0; q < kBatch; ++q) {
+          const int i = i0 + q * kThreads;
+          u[q] = i < nv ? __ldcs(vr + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+          const int i = i0 + q * kThreads;
+          if (i < nv) {
+            float x[VEC];
+            Row<Tin>::unpack(u[q], x);
+            float vmax = x[0];
+#pragma unroll
+            for (int j = 1; j < VEC; ++j) vmax = fmaxf(vmax, x[j]);
+            if (vmax >= tau) {
+#pragma unroll
+              for (int j = 0; j < VEC; ++j) {
+                if (x[j] >= tau) {
+                  const int p = atomicAdd(&sm_n, 1);
+                  if (p < kCandCap) cand[p] = rkey(x[j], (uint32_t)(rs.head + i * VEC + j));
+                }
+              }
+            }
+          }
+        }
+      }
       __syncthreads();
-      const int nsel = sm_misc[3];
-      if (kth == 0 || nsel > kSelCap || nsel < K) {
+      const int n = sm_n;
+      if (n > kCandCap || n < K) {
         exact = true;
       } else {
         int n2 = 1;
-        while (n2 < nsel) n2 <<= 1;
-        for (int i = nsel + tid; i < n2; i += kThreads) sel[i] = 0;
+        while (n2 < n) n2 <<= 1;
+        for (int i = n + tid; i < n2; i += kThreads) cand[i] = 0;
         __syncthreads();
-        bitonic_desc(sel, n2);
-        const uint64_t eK = sel[K - 1];
-        const float eKv = okey_to_float((uint32_t)(eK >> 32));
-        const bool ok = eK != 0 && st.drop < eK && st.drop_v < eKv;
-        exact = !__syncthreads_and(ok);
+        bitonic_desc(cand, n2);
       }
     }
     if (exact) {
       if (tid == 0 && !force_exact) atomicAdd(&ws_words[1], 1);
       __syncthreads();
-      exact_select<Tin>(rp, V, K, sel, sel_n, hist, sm_scan, sm_misc);
+      int kp2 = 1;
+      while (kp2 < K) kp2 <<= 1;  // <= sel_entries(K)
+      exact_select<Tin>(rp, V, K, cand, kp2, hist, sm_scan, sm_misc);
     }
     __syncthreads();
     const float lse = sm_lse;
     for (int k = tid; k < K; k += kThreads) {
-      const uint64_t c = sel[k];
+      const uint64_t c = cand[k];
       ids[(int64_t)row * K + k] = (int32_t)(0xFFFFFFFFu - (uint32_t)c);
       logp[(int64_t)row * K + k] = okey_to_float((uint32_t)(c >> 32)) - lse;
     }
     __syncthreads();
+    row = sm_next;
+    __syncthreads();
   }
-}
-
-int sel_entries(int K) {
-  int n = 1;
-  while (n < K) n <<= 1;
-  return n < kSelCap ? kSelCap : n;
 }
 
 }  // namespace
 
-size_t topk_smem_bytes(int K) { return (size_t)kStages * kChunk + (size_t)sel_entries(K) * sizeof(uint64_t); }
+// Entries of the candidate / exact-path buffer: the fast path's candidate
+// buffer, or a power of two >= K for the exact path if larger.
+static int sel_entries(int K) {
+  int n = 1;
+  while (n < K) n <<= 1;
+  return n < kCandCap ? kCandCap : n;
+}
+
+size_t topk_smem_bytes(int K) { return (size_t)sel_entries(K) * sizeof(uint64_t); }
 
 cudaError_t launch_topk(const void* logits, int dtype, int64_t T, int64_t V, int64_t ld, int K,
                         int32_t* ids, float* logp, int* ws_words, int force_exact, int num_sms,
                         cudaStream_t stream) {
-  const int n = sel_entries(K);
   const size_t smem = topk_smem_bytes(K);
   int blocks_per_sm = 0;
   cudaError_t e = cudaMemsetAsync(ws_words + 2, 0, sizeof(int), stream);  // row counter
@@ -589,14 +496,15 @@ cudaError_t launch_topk(const void* logits, int dtype, int64_t T, int64_t V, int
   }
   if (e != cudaSuccess) return e;
   if (blocks_per_sm < 1) blocks_per_sm = 1;
+  if (blocks_per_sm > 2) blocks_per_sm = 2;  // rows in flight must stay in L2 for pass 2
   int64_t grid = (int64_t)num_sms * blocks_per_sm;
   if (grid > T) grid = T;
   if (dtype == 0)
     topk_kernel<uint16_t><<<(unsigned)grid, kThreads, smem, stream>>>(
-        static_cast<const uint16_t*>(logits), T, (int)V, ld, K, n, force_exact, ids, logp, ws_words);
+        static_cast<const uint16_t*>(logits), T, (int)V, ld, K, force_exact, ids, logp, ws_words);
   else
     topk_kernel<float><<<(unsigned)grid, kThreads, smem, stream>>>(
-        static_cast<const float*>(logits), T, (int)V, ld, K, n, force_exact, ids, logp, ws_words);
+        static_cast<const float*>(logits), T, (int)V, ld, K, force_exact, ids, logp, ws_words);
   return cudaGetLastError();
 }
 
