@@ -5,19 +5,21 @@
 // teacher runs once and only its K most probable tokens per position are
 // kept). Selection order: value descending, then id ascending; -0.0 == +0.0.
 //
-// Persistent CTAs (two per SM) take rows from an atomic counter; per row:
+// Persistent CTAs (three per SM) take rows from an atomic counter; per row:
 //   pass 1  stream the row from HBM with 16-byte loads (8 per thread in
 //           flight). Each thread keeps an online (max, sum of exp) of its
 //           elements. That is the log-sum-exp, merged in a fixed order
-//           (deterministic), and its max is a statistic for the selection.
+//           (deterministic). It also records the maximum of each batch of 8
+//           vectors in shared memory.
 //   tau     the K-th largest of the 256 per-thread maxima, found by a
 //           bisection over the value keys (one __syncthreads_count per bit).
 //           The maxima are K distinct elements >= tau, so tau is a lower
 //           bound of the row's K-th largest value. On the pages' workload only
 //           about 200 elements of a 201088-wide row are >= tau.
-//   pass 2  re-read the row (now in L2, loads marked evict-first) and append
-//           every element >= tau to a shared buffer. It holds every top-K
-//           element, ties included.
+//   pass 2  each thread re-reads only its batches of 8 vectors whose maximum
+//           (recorded in pass 1) is >= tau, about 6% of the row, and appends
+//           every element >= tau to a shared buffer. The buffer holds every
+//           top-K element, ties included.
 //   select  sort the buffer by (value desc, id asc); its first K entries are
 //           the cache row.
 // If the buffer overflows (massive ties) or K > 1024, the row is redone by an
@@ -36,6 +38,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kCandCap = 2048;   // candidate buffer entries (fast path)
 constexpr int kFastMaxK = 1024;  // larger K goes to the exact path
 constexpr int kBatch = 8;        // 16-byte loads per thread in flight in pass 1
+constexpr int kSlots = 16;       // per-thread batch-maximum slots kept for pass 2
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -308,7 +311,7 @@ __device__ void exact_select(const Tin* row, int V, int K, uint64_t* cand, int n
 }
 
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads, 2) topk_kernel(const Tin* __restrict__ logits, int64_t T, int V,
+__global__ void __launch_bounds__(kThreads, 3) topk_kernel(const Tin* __restrict__ logits, int64_t T, int V,
                                                            int64_t ld, int K, int force_exact,
                                                            int32_t* __restrict__ ids, float* __restrict__ logp,
                                                            int* __restrict__ ws_words) {
@@ -321,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const Tin* __restrict
   __shared__ float sm_lse;
   __shared__ int sm_n;
   __shared__ int sm_next;
+  __shared__ float bmax[kSlots][kThreads];  // per-thread batch maxima (batch b in slot b % kSlots)
 
   constexpr int VEC = Row<Tin>::kVec;
   constexpr int kLoBits = sizeof(Tin) == 2 ? 16 : 0;
@@ -344,13 +348,17 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const Tin* __restrict
     st.init();
     if (tid < rs.head) st.one(Row<Tin>::cvt(rp[tid]));
     if (tid < rs.tail) st.one(Row<Tin>::cvt(rp[rs.tail0 + tid]));
-    for (int i0 = tid; i0 < nv; i0 += kBatch * kThreads) {
+#pragma unroll
+    for (int q = 0; q < kSlots; ++q) bmax[q][tid] = -INFINITY;
+    int nb = 0;  // batches of this thread
+    for (int i0 = tid; i0 < nv; i0 += kBatch * kThreads, ++nb) {
       uint4 u[kBatch];
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         const int i = i0 + q * kThreads;
-        u[q] = i < nv ? __ldg(vr + i) : make_uint4(0u, 0u, 0u, 0u);
+        u[q] = i < nv ? __ldcs(vr + i) : make_uint4(0u, 0u, 0u, 0u);
       }
+      float bm = -INFINITY;
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         if (i0 + q * kThreads < nv) {
@@ -360,8 +368,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const Tin* __restrict
 #pragma unroll
           for (int j = 1; j < VEC; ++j) vmax = fmaxf(vmax, x[j]);
           st.add(x, vmax);
+          bm = fmaxf(bm, vmax);
         }
       }
+      const int slot = nb % kSlots;
+      bmax[slot][tid] = fmaxf(bmax[slot][tid], bm);
     }
     float m = st.m, sum = st.s;
 #pragma unroll
@@ -406,7 +417,10 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const Tin* __restrict
           if (p < kCandCap) cand[p] = rkey(x, (uint32_t)(rs.tail0 + tid));
         }
       }
-      for (int i0 = tid; i0 < nv; i0 += kBatch * kThreads) {
+      // only batches whose recorded maximum reaches tau (threads whose
+      // maximum is below tau read nothing)
+      for (int bi = 0, i0 = tid; st.m >= tau && i0 < nv; i0 += kBatch * kThreads, ++bi) {
+        if (bmax[bi % kSlots][tid] < tau) continue;
         uint4 u[kBatch];
 #pragma unroll
         for (int q = 0; q < kBatch; ++q) {
@@ -496,7 +510,6 @@ cudaError_t launch_topk(const void* logits, int dtype, int64_t T, int64_t V, int
   }
   if (e != cudaSuccess) return e;
   if (blocks_per_sm < 1) blocks_per_sm = 1;
-  if (blocks_per_sm > 2) blocks_per_sm = 2;  // rows in flight must stay in L2 for pass 2
   int64_t grid = (int64_t)num_sms * blocks_per_sm;
   if (grid > T) grid = T;
   if (dtype == 0)
