@@ -26,6 +26,13 @@ extern "C" {
 KD_API int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int32_t a_mn,
                         int32_t b_mn, int32_t flags, void* ws, void* stream);
 
+/* Launches a one-warp kernel that waits on an mbarrier nothing arrives at,
+ * with the bounded wait all libkd pipelines use, here limited to limit_ns
+ * (0 < limit_ns <= 1e10). When the limit passes, the kernel writes
+ * KD_ERR_DEVICE_TIMEOUT into the status word at ws and returns normally, so
+ * the context stays usable. Read the word with kd_read_device_status. */
+KD_API int kd_test_wait_timeout(int64_t limit_ns, void* ws, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

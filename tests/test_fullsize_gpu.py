@@ -1,0 +1,102 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py
+times (same T, d, V, K and chunk).
+
+The full fp64 oracle over all T positions is out of reach here (up to 1e15
+flops), so:
+  * lse, the per-position loss L_t and dH_t are compared on a seeded sample
+    of positions. It includes the first and last positions and chunk
+    boundaries, and the oracle computes each sampled row on its own;
+  * the scalar loss must equal the mean of the per-position losses, a
+    property that holds at any size;
+  * dW (a sum over all positions) is compared in full on a T-truncated run
+    with the same d, V and chunk: two chunks plus a ragged tail of 37
+    positions (one chunk plus the tail for the long-context workload).
+The teacher cache is synthetic (K distinct ids per row), so that no oracle
+input comes from the CUDA path.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import top_kl_loss_tcgen05_b300 as kd
+from oracle import kd_oracle as O
+from top_kl_loss_tcgen05_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+LOSS_RTOL = 1e-3
+GRAD_RTOL = 1e-2
+
+
+def frob(a, b):
+    return float(np.linalg.norm(np.asarray(a, np.float64) - b) / np.linalg.norm(b))
+
+
+def _inputs(name, T=None):
+    c = synth.CONFIGS[name]
+    T = c["T"] if T is None else T
+    dev = torch.device("cuda:0")
+    H, W = synth.student(T, c["d"], c["V"], c["seed"], device=dev)
+    ids, logp = synth.synthetic_cache(T, c["V"], c["K"], c["seed"])
+    return c, H, W, ids.to(dev), logp.to(dev)
+
+
+def _sample_rows(T, chunk, n=64, seed=0):
+    rng = np.random.default_rng(seed)
+    fixed = [0, T - 1, chunk - 1, chunk, min(T - 1, 2 * chunk - 1)]
+    rows = set(int(r) for r in fixed if 0 <= r < T)
+    while len(rows) < n:
+        rows.add(int(rng.integers(T)))
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("name", ["llama3b", "gptoss20b", "long"])
+def test_full_size_sampled_positions(cuda_dev, name):
+    c, H, W, ids, logp = _inputs(name)
+    T, chunk = c["T"], c["chunk"]
+    loss, lse, rows = kd.fused_kl_fwd(H, W, ids, logp, chunk, want_rows=True)
+    dH, _ = kd.fused_kl_bwd(H, W, ids, logp, lse, chunk, 1.0 / T)
+    torch.cuda.synchronize()
+    lse_g = lse.cpu().numpy()
+    rows_g = rows.cpu().numpy().astype(np.float64)
+    # scalar loss = mean of per-position losses (any size)
+    assert abs(loss.item() - rows_g.mean()) <= 1e-6 * abs(rows_g.mean())
+    assert np.all(np.isfinite(rows_g)) and np.all(rows_g > -1e-3)  # Gibbs: KL >= 0
+    # oracle on sampled positions
+    S = _sample_rows(T, chunk)
+    St = torch.as_tensor(S, device=cuda_dev)
+    Hs = H[St].float().cpu().numpy()
+    W64 = W.float().cpu().numpy().astype(np.float64)
+    ids_s, logp_s = ids[St].cpu().numpy(), logp[St].cpu().numpy()
+    _, lse_o, L_o = O.fused_kl_forward(Hs, W64, ids_s, logp_s)
+    dH_o, _ = O.fused_kl_backward(Hs, W64, ids_s, logp_s, 1.0 / T)
+    np.testing.assert_allclose(lse_g[S], lse_o, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(rows_g[S], L_o, rtol=LOSS_RTOL, atol=1e-4)
+    assert abs(rows_g[S].mean() - L_o.mean()) <= LOSS_RTOL * abs(L_o.mean())
+    assert frob(dH[St].cpu().numpy(), dH_o) <= GRAD_RTOL
+
+
+@pytest.mark.parametrize("name", ["llama3b", "gptoss20b", "long"])
+def test_full_width_dW_on_truncated_run(cuda_dev, name):
+    c = synth.CONFIGS[name]
+    chunk = c["chunk"]
+    Tp = (chunk + 37) if name == "long" else (2 * chunk + 37)
+    c, H, W, ids, logp = _inputs(name, T=Tp)
+    _, lse, _ = kd.fused_kl_fwd(H, W, ids, logp, chunk)
+    dH, dW = kd.fused_kl_bwd(H, W, ids, logp, lse, chunk, 1.0 / Tp)
+    torch.cuda.synchronize()
+    # oracle: dW = sum_t g_t h_t^T, positions in blocks of 256 (host memory)
+    H64 = H.float().cpu().numpy().astype(np.float64)
+    W64 = W.float().cpu().numpy().astype(np.float64)
+    idn, lpn = ids.cpu().numpy(), logp.cpu().numpy()
+    dW_o = np.zeros_like(W64)
+    dH_o = np.empty_like(H64)
+    for t0 in range(0, Tp, 256):
+        t1 = min(Tp, t0 + 256)
+        z = O.student_logits(H64[t0:t1], W64)
+        g = O.dlogits(z, idn[t0:t1], lpn[t0:t1], 1.0 / Tp)
+        dW_o += g.T @ H64[t0:t1]
+        dH_o[t0:t1] = g @ W64
+    assert frob(dW.cpu().numpy(), dW_o) <= GRAD_RTOL
+    assert frob(dH.cpu().numpy(), dH_o) <= GRAD_RTOL

@@ -45,6 +45,7 @@ SIGNATURES = {
     ),
     "kd_read_device_status": (ctypes.c_int, [_P, _P]),
     "kd_test_gemm": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32, _P, _P]),
+    "kd_test_wait_timeout": (ctypes.c_int, [_I64, _P, _P]),
     "kd_profile_begin": (ctypes.c_int, []),
     "kd_profile_end": (ctypes.c_int, [_P, _I32, _P]),
 }

@@ -428,6 +428,11 @@ int kd_read_device_status(void* ws, void* stream) {
   return v;
 }
 
+int kd_test_wait_timeout(int64_t limit_ns, void* ws, void* stream) {
+  if (!ws || limit_ns <= 0 || limit_ns > 10000000000ll) return KD_ERR_INVALID_ARG;
+  return cuda_status(launch_wait_timeout((uint64_t)limit_ns, static_cast<int*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
 int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int32_t a_mn,
                  int32_t b_mn, int32_t flags, void* ws, void* stream) {
   if (!A || !B || !C || !ws || M <= 0 || N <= 0 || K <= 0) return KD_ERR_INVALID_ARG;

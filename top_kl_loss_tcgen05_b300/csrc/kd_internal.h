@@ -69,6 +69,7 @@ cudaError_t launch_merge(const float* part_m, const float* part_s, int S, int ro
 cudaError_t launch_chunk_reduce(const double* block_sums, int nblocks, double* acc, int first, cudaStream_t s);
 cudaError_t launch_finalize(const double* acc, double inv_T, float* loss, cudaStream_t s);
 cudaError_t launch_transpose(const void* src, int rows, int cols, void* dst, int ld_dst, cudaStream_t s);
+cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 
 // Top-K (kd_topk.cu).
 size_t topk_smem_bytes(int K);

@@ -219,7 +219,24 @@ __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t* __restri
   }
 }
 
+// Waits on an mbarrier that nothing arrives at, with a time limit, and
+// records the timeout in the status word: the failure path every pipeline
+// wait takes, exercised on purpose.
+__global__ void wait_timeout_kernel(uint64_t limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_for(&bar, 0u, limit_ns)) set_status(status, ST_TIMEOUT);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s) {
+  wait_timeout_kernel<<<1, 32, 0, s>>>(limit_ns, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_transpose(const void* src, int rows, int cols, void* dst, int ld_dst, cudaStream_t s) {
   dim3 grid((cols + 31) / 32, (rows + 31) / 32);
