@@ -403,11 +403,12 @@ def main():
     if status != 0:
         raise RuntimeError("device status %s in the timed region" % _native.status_string(status))
 
-    # dominant kernel and its roofline (algorithmic flops per launch / mean launch time)
-    nchunks = (T + chunk - 1) // chunk
-    flops_per_launch = {"logits_fwd_lse_gather": 2.0 * T * d * V / nchunks,
-                        "logits_dz": 2.0 * T * d * V / nchunks,
-                        "grad_dH_dW": 4.0 * T * d * V / nchunks}
+    # dominant kernel and its roofline (algorithmic flops per launch / mean
+    # launch time). Per step: logits 2TdV, recompute 2TdV, dH + dW 4TdV,
+    # spread over however many launches each kernel made.
+    flops_per_step = {"logits_fwd_lse_gather": 2.0 * T * d * V, "logits_dz": 2.0 * T * d * V,
+                      "grad_dH_dW": 4.0 * T * d * V}
+    flops_per_launch = {k: f * args.steps / prof[k][0] for k, f in flops_per_step.items() if k in prof}
     total_kernel_ms = sum(v[1] for v in prof.values())
     dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
     kernels = {k: {"launches": n, "ms_per_step": t / args.steps, "share": t / total_kernel_ms if total_kernel_ms else 0.0}

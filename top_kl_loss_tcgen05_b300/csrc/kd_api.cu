@@ -57,9 +57,15 @@ int num_sms_current() {
   return n;
 }
 
+// The backward pass groups chunks for its dH/dW GEMM when chunks are small:
+// the fp32 dW read-modify-write (8 V d bytes) then happens once per group
+// instead of once per chunk. The workspace holds the group's dz.
+int64_t bwd_group(int64_t chunk) { return chunk < 2048 ? 2 : 1; }
+
 // Fused-loss workspace layout (all offsets 256-byte aligned; dz 1024).
 struct Layout {
   int Kp;
+  int64_t G;    // chunks per dH/dW group (backward)
   int64_t S;    // vocabulary tiles of the forward GEMM
   int64_t ldz;  // dz row stride in elements
   int64_t ldt;  // row stride of the transposed hidden-state chunk
@@ -71,7 +77,8 @@ Layout fused_layout(int64_t d, int64_t V, int K, int64_t chunk) {
   L.Kp = (K + 3) / 4 * 4;
   L.S = ceil_div(V, kBNLogits);
   L.ldz = align_up((size_t)V, 64);
-  L.ldt = align_up((size_t)chunk, 64);
+  L.G = bwd_group(chunk);
+  L.ldt = align_up((size_t)(L.G * chunk), 64);
   size_t o = kHeader;
   auto take = [&](size_t bytes, size_t al) {
     o = align_up(o, al);
@@ -88,7 +95,7 @@ Layout fused_layout(int64_t d, int64_t V, int K, int64_t chunk) {
   L.part_m = take((size_t)L.S * chunk * 4, 256);
   L.part_s = take((size_t)L.S * chunk * 4, 256);
   L.hct = take((size_t)d * L.ldt * 2, 1024);
-  L.dz = take((size_t)chunk * L.ldz * 2, 1024);
+  L.dz = take((size_t)(L.G * chunk) * L.ldz * 2, 1024);
   L.total = align_up(o, 256);
   return L;
 }
@@ -336,73 +343,78 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
                     32);
   if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
 
-  for (int64_t c0 = 0; c0 < T; c0 += chunk) {
-    const int rows = (int)((T - c0) < chunk ? (T - c0) : chunk);
-    {
-      ProfScope ps(K_PREP, s);
-      e = launch_prep(ids + c0 * K, logp + c0 * K, rows, K, (int)V, L.Kp, ids_sorted, p_sorted, cnt, ent, status, s);
-    }
-    if (e != cudaSuccess) return cuda_status(e);
+  const int64_t gchunk = L.G * chunk;
+  for (int64_t g0 = 0; g0 < T; g0 += gchunk) {
+    const int grows = (int)((T - g0) < gchunk ? (T - g0) : gchunk);
+    for (int64_t c0 = g0; c0 < g0 + grows; c0 += chunk) {
+      const int rows = (int)((T - c0) < chunk ? (T - c0) : chunk);
+      {
+        ProfScope ps(K_PREP, s);
+        e = launch_prep(ids + c0 * K, logp + c0 * K, rows, K, (int)V, L.Kp, ids_sorted, p_sorted, cnt, ent, status,
+                        s);
+      }
+      if (e != cudaSuccess) return cuda_status(e);
 
-    // Recompute the chunk's logits; the epilogue writes dz (bf16).
-    if (encode_map_2d(&az.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + c0 * d, (uint64_t)d, (uint64_t)rows,
-                      (uint64_t)d * 2, kBK, kBM) != cudaSuccess ||
-        encode_map_2d(&az.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)rows,
-                      (uint64_t)L.ldz * 2, 64, 32) != cudaSuccess)
-      return KD_ERR_UNSUPPORTED;
-    {
-      Problem& P = az.pr[0];
-      P.m_blocks = (int)ceil_div(rows, kBM);
-      P.n_blocks = (int)ceil_div(V, kBNLogits);
-      P.k_blocks = (int)ceil_div(d, kBK);
-      P.a_mn = 0; P.b_mn = 0; P.M = rows; P.N = (int)V;
-      P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
-      az.nprob = 1;
-      az.total_tiles = P.m_blocks * P.n_blocks;
-      az.rows = rows; az.row_stride = (int)chunk; az.V = (int)V; az.Kp = L.Kp;
-      az.ids_sorted = ids_sorted; az.p_sorted = p_sorted; az.cnt = cnt;
-      az.lse = lse + c0; az.scale = grad_scale; az.dscale = grad_scale_dev;
-      az.status = status;
-      az.tile_counter = counter;
+      // Recompute the chunk's logits; the epilogue writes its rows of dz (bf16).
+      if (encode_map_2d(&az.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + c0 * d, (uint64_t)d, (uint64_t)rows,
+                        (uint64_t)d * 2, kBK, kBM) != cudaSuccess ||
+          encode_map_2d(&az.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz + (c0 - g0) * L.ldz, (uint64_t)V,
+                        (uint64_t)rows, (uint64_t)L.ldz * 2, 64, 32) != cudaSuccess)
+        return KD_ERR_UNSUPPORTED;
+      {
+        Problem& P = az.pr[0];
+        P.m_blocks = (int)ceil_div(rows, kBM);
+        P.n_blocks = (int)ceil_div(V, kBNLogits);
+        P.k_blocks = (int)ceil_div(d, kBK);
+        P.a_mn = 0; P.b_mn = 0; P.M = rows; P.N = (int)V;
+        P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
+        az.nprob = 1;
+        az.total_tiles = P.m_blocks * P.n_blocks;
+        az.rows = rows; az.row_stride = (int)chunk; az.V = (int)V; az.Kp = L.Kp;
+        az.ids_sorted = ids_sorted; az.p_sorted = p_sorted; az.cnt = cnt;
+        az.lse = lse + c0; az.scale = grad_scale; az.dscale = grad_scale_dev;
+        az.status = status;
+        az.tile_counter = counter;
+      }
+      {
+        ProfScope ps(K_LOGITS_DZ, s);
+        e = launch_logits_dz(az, sms, s);
+      }
+      if (e != cudaSuccess) return cuda_status(e);
     }
-    {
-      ProfScope ps(K_LOGITS_DZ, s);
-      e = launch_logits_dz(az, sms, s);
-    }
-    if (e != cudaSuccess) return cuda_status(e);
 
-    // H_c^T [d, rows] (K-major B operand of the dW GEMM).
+    // H_g^T [d, grows] (K-major B operand of the dW GEMM).
     {
       ProfScope ps(K_TRANSPOSE, s);
-      e = launch_transpose(Hb + c0 * d, rows, (int)d, hct, (int)L.ldt, s);
+      e = launch_transpose(Hb + g0 * d, grows, (int)d, hct, (int)L.ldt, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
 
-    // dH_c^T = W^T dz^T (problem 0, stored transposed into dH) and
-    // dW (+)= dz^T H_c (problem 1), one launch.
-    if (encode_map_2d(&ag.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)rows,
+    // dH_g^T = W^T dz^T (problem 0, stored transposed into dH) and
+    // dW (+)= dz^T H_g (problem 1), one launch over the group's positions.
+    if (encode_map_2d(&ag.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
                       (uint64_t)L.ldz * 2, kBK, kBNGrad) != cudaSuccess ||
-        encode_map_2d(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dH + c0 * d, (uint64_t)d, (uint64_t)rows,
+        encode_map_2d(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dH + g0 * d, (uint64_t)d, (uint64_t)grows,
                       (uint64_t)d * 4, 32, 32) != cudaSuccess ||
-        encode_map_2d(&ag.tmA[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)rows,
+        encode_map_2d(&ag.tmA[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
                       (uint64_t)L.ldz * 2, 64, 64) != cudaSuccess ||
-        encode_map_2d(&ag.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, hct, (uint64_t)rows, (uint64_t)d,
+        encode_map_2d(&ag.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, hct, (uint64_t)grows, (uint64_t)d,
                       (uint64_t)L.ldt * 2, kBK, kBNGrad) != cudaSuccess)
       return KD_ERR_UNSUPPORTED;
     {
       Problem& P0 = ag.pr[0];
       P0.m_blocks = (int)ceil_div(d, kBM);
-      P0.n_blocks = (int)ceil_div(rows, kBNGrad);
+      P0.n_blocks = (int)ceil_div(grows, kBNGrad);
       P0.k_blocks = (int)ceil_div(V, kBK);
-      P0.a_mn = 1; P0.b_mn = 0; P0.M = (int)d; P0.N = rows;
+      P0.a_mn = 1; P0.b_mn = 0; P0.M = (int)d; P0.N = grows;
       P0.tile_begin = 0; P0.n_fastest = 0; P0.reduce_add = 0; P0.c_trans = 1;
       Problem& P1 = ag.pr[1];
       P1.m_blocks = (int)ceil_div(V, kBM);
       P1.n_blocks = (int)ceil_div(d, kBNGrad);
-      P1.k_blocks = (int)ceil_div(rows, kBK);
+      P1.k_blocks = (int)ceil_div(grows, kBK);
       P1.a_mn = 1; P1.b_mn = 0; P1.M = (int)V; P1.N = (int)d;
       P1.tile_begin = P0.m_blocks * P0.n_blocks; P1.n_fastest = 1;
-      P1.reduce_add = (accumulate_dW || c0 > 0) ? 1 : 0;
+      P1.reduce_add = (accumulate_dW || g0 > 0) ? 1 : 0;
       P1.c_trans = 0;
       ag.nprob = 2;
       ag.total_tiles = P1.tile_begin + P1.m_blocks * P1.n_blocks;
