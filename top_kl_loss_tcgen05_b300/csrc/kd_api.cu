@@ -34,6 +34,7 @@ namespace {
 constexpr size_t kHeader = 256;  // status word, counters, fp64 loss accumulator
 constexpr size_t kCounterOffset = 64;  // int: tile counter of the GEMM launches
 constexpr size_t kAccOffset = 128;
+constexpr size_t kDoneOffset = 136;    // unsigned: blocks of the current merge launch that finished
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -91,7 +92,7 @@ Layout fused_layout(int64_t d, int64_t V, int K, int64_t chunk) {
   L.cnt = take((size_t)chunk * 4, 256);
   L.ent = take((size_t)chunk * 4, 256);
   L.zK = take((size_t)chunk * L.Kp * 4, 256);
-  L.block_sums = take((size_t)ceil_div(chunk, 32) * 8, 256);
+  L.block_sums = take((size_t)ceil_div(chunk, 8) * 8, 256);
   L.part_m = take((size_t)L.S * chunk * 4, 256);
   L.part_s = take((size_t)L.S * chunk * 4, 256);
   L.hct = take((size_t)d * L.ldt * 2, 1024);
@@ -105,11 +106,11 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // ------------------------------------------------------------------ profiling
 // Kernel names reported by kd_profile_end, indexed by KernelId.
 enum KernelId {
-  K_TOPK, K_PREP, K_LOGITS_FWD, K_MERGE, K_REDUCE, K_FINALIZE, K_LOGITS_DZ, K_TRANSPOSE, K_GRAD, K_TEST, K_COUNT
+  K_TOPK, K_PREP, K_LOGITS_FWD, K_MERGE, K_FINALIZE, K_LOGITS_DZ, K_TRANSPOSE, K_GRAD, K_TEST, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {"topk_cache", "teacher_prep", "logits_fwd_lse_gather", "lse_merge_loss",
-                                           "loss_chunk_reduce", "loss_finalize", "logits_dz", "hidden_transpose",
-                                           "grad_dH_dW", "test_gemm"};
+                                           "loss_finalize", "logits_dz", "hidden_transpose", "grad_dH_dW",
+                                           "test_gemm"};
 struct ProfRec {
   int kid;
   cudaEvent_t a, b;
@@ -245,6 +246,7 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
   uint8_t* w = static_cast<uint8_t*>(ws);
   int* status = reinterpret_cast<int*>(w);
   double* acc = reinterpret_cast<double*>(w + kAccOffset);
+  unsigned* done = reinterpret_cast<unsigned*>(w + kDoneOffset);
   int* ids_sorted = reinterpret_cast<int*>(w + L.ids_sorted);
   float* p_sorted = reinterpret_cast<float*>(w + L.p_sorted);
   int* cnt = reinterpret_cast<int*>(w + L.cnt);
@@ -254,6 +256,10 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
   float* part_m = reinterpret_cast<float*>(w + L.part_m);
   float* part_s = reinterpret_cast<float*>(w + L.part_s);
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
+  // The merge kernels count finished blocks in the workspace header; the
+  // count returns to 0 after every launch, and starts there for this call.
+  cudaError_t e0 = cudaMemsetAsync(done, 0, sizeof(unsigned), s);
+  if (e0 != cudaSuccess) return cuda_status(e0);
 
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -279,7 +285,7 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
     P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0;
     a.nprob = 1;
     a.total_tiles = P.m_blocks * P.n_blocks;
-    a.rows = rows; a.row_stride = (int)chunk; a.V = (int)V; a.Kp = L.Kp;
+    a.rows = rows; a.row_stride = (int)chunk; a.S = (int)L.S; a.V = (int)V; a.Kp = L.Kp;
     a.ids_sorted = ids_sorted; a.p_sorted = p_sorted; a.cnt = cnt;
     a.zK = zK; a.part_m = part_m; a.part_s = part_s;
     a.status = status;
@@ -291,13 +297,8 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
     if (e != cudaSuccess) return cuda_status(e);
     {
       ProfScope ps(K_MERGE, s);
-      e = launch_merge(part_m, part_s, (int)L.S, rows, (int)chunk, ent, p_sorted, zK, cnt, L.Kp, lse + c0,
-                       loss_rows ? loss_rows + c0 : nullptr, bsum, s);
-    }
-    if (e != cudaSuccess) return cuda_status(e);
-    {
-      ProfScope ps(K_REDUCE, s);
-      e = launch_chunk_reduce(bsum, (int)ceil_div(rows, 32), acc, c0 == 0, s);
+      e = launch_merge(part_m, part_s, (int)L.S, rows, ent, p_sorted, zK, cnt, L.Kp, lse + c0,
+                       loss_rows ? loss_rows + c0 : nullptr, bsum, done, acc, c0 == 0, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
   }

@@ -336,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
         if (row < g.rows) {
-          g.part_m[(size_t)tl.nb * g.row_stride + row] = m;
-          g.part_s[(size_t)tl.nb * g.row_stride + row] = s;
+          g.part_m[(size_t)row * g.S + tl.nb] = m;
+          g.part_s[(size_t)row * g.S + tl.nb] = s;
         }
       } else if (EPI == EPI_DZ) {
         const float lse_r = (row < g.rows) ? __ldg(g.lse + row) : 0.f;

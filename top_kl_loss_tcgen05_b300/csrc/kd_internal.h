@@ -37,15 +37,16 @@ struct GemmArgs {
   int* tile_counter;      // dynamic tile scheduler (zeroed before each launch)
   // fused-epilogue data (chunk-local rows)
   int rows;               // rows of this chunk
-  int row_stride;         // stride of the [S][chunk] partial arrays (= chunk)
+  int row_stride;         // chunk (rows of the per-chunk arrays)
+  int S;                  // vocabulary tiles: row stride of the [chunk][S] partials
   int V;
   int Kp;                 // row stride of the sorted id / p / zK arrays
   const int* ids_sorted;  // [chunk][Kp], ascending, padded
   const float* p_sorted;  // [chunk][Kp]
   const int* cnt;         // [chunk] entries per row
   float* zK;              // [chunk][Kp] student logit at each sorted id
-  float* part_m;          // [S][chunk] per-(row, vocab tile) max
-  float* part_s;          // [S][chunk] per-(row, vocab tile) sum exp(z - max)
+  float* part_m;          // [chunk][S] per-(row, vocab tile) max
+  float* part_s;          // [chunk][S] per-(row, vocab tile) sum exp(z - max)
   const float* lse;       // [rows] chunk slice of the saved log-sum-exp
   float scale;            // dz scale
   const float* dscale;    // optional device multiplier of `scale`
@@ -63,10 +64,10 @@ cudaError_t launch_grad(const GemmArgs& a, int num_sms, cudaStream_t s);
 // Small kernels (kd_loss_aux.cu).
 cudaError_t launch_prep(const int32_t* ids, const float* logp, int rows, int K, int V, int Kp, int* ids_sorted,
                         float* p_sorted, int* cnt, float* ent, int* status, cudaStream_t s);
-cudaError_t launch_merge(const float* part_m, const float* part_s, int S, int rows, int row_stride,
-                         const float* ent, const float* p_sorted, const float* zK, const int* cnt, int Kp,
-                         float* lse_out, float* loss_rows_out, double* block_sums, cudaStream_t s);
-cudaError_t launch_chunk_reduce(const double* block_sums, int nblocks, double* acc, int first, cudaStream_t s);
+cudaError_t launch_merge(const float* part_m, const float* part_s, int S, int rows, const float* ent,
+                         const float* p_sorted, const float* zK, const int* cnt, int Kp, float* lse_out,
+                         float* loss_rows_out, double* block_sums, unsigned* done, double* acc, int first,
+                         cudaStream_t s);
 cudaError_t launch_finalize(const double* acc, double inv_T, float* loss, cudaStream_t s);
 cudaError_t launch_transpose(const void* src, int rows, int cols, void* dst, int ld_dst, cudaStream_t s);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s);

@@ -8,8 +8,8 @@
 //  merge   per position: log-sum-exp over the whole vocabulary from the
 //          per-tile (max, sum) partials of the forward GEMM; the loss
 //          L_t = sum p log p - sum_k p_k z_id_k + lse_t; a per-block sum.
-//  reduce  the chunk's block sums, added to the running fp64 total in a fixed
-//          order, and finally loss = total / T.
+//          The last block of a chunk adds the chunk's block sums to the
+//          running fp64 total in a fixed order; finally loss = total / T.
 // All reductions run in a fixed order, so the loss is bitwise reproducible.
 // Definition: "ทำให้ Knowledge Distillation มีประสิทธิภาพ..." (ai-thai.com),
 // section "กลไก Fused Chunked KL Loss". The KL direction, the
@@ -146,55 +146,76 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   m = mm;
 }
 
-// 256 threads, 32 positions per block: warp w merges vocabulary tiles
-// w, w+8, ... for its 32 positions; warp 0 then merges the 8 results.
+// One warp per position, 8 positions per block. Each lane merges every 32nd
+// vocabulary-tile partial of the row (a coalesced read of the row's [S]
+// partials), then the lanes are combined by an xor-shuffle tree. The merge
+// is commutative, so every lane ends with the same value. The block sum of
+// its 8 losses is taken in a fixed order, so the result is deterministic.
 __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ part_m,
                                                     const float* __restrict__ part_s, int S, int rows,
-                                                    int row_stride, const float* __restrict__ ent,
+                                                    const float* __restrict__ ent,
                                                     const float* __restrict__ p_sorted,
                                                     const float* __restrict__ zK, const int* __restrict__ cnt,
                                                     int Kp, float* __restrict__ lse_out,
                                                     float* __restrict__ loss_rows_out,
-                                                    double* __restrict__ block_sums) {
-  __shared__ float sm[8][32], ss[8][32];
-  __shared__ float sl[32];
+                                                    double* __restrict__ block_sums, unsigned* done,
+                                                    double* acc, int first) {
+  __shared__ float sl[8];
+  __shared__ bool last_block;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const int row = blockIdx.x * 32 + lane;
-  float m = -INFINITY, s = 0.f;
+  const int row = blockIdx.x * 8 + w;
+  float L = 0.f;
   if (row < rows) {
-    for (int j = w; j < S; j += 8) lse_merge(m, s, part_m[(size_t)j * row_stride + row], part_s[(size_t)j * row_stride + row]);
-  }
-  sm[w][lane] = m;
-  ss[w][lane] = s;
-  __syncthreads();
-  if (w == 0) {
-    float M = sm[0][lane], Ssum = ss[0][lane];
-    for (int q = 1; q < 8; ++q) lse_merge(M, Ssum, sm[q][lane], ss[q][lane]);
-    float L = 0.f;
-    if (row < rows) {
-      const float lse = M + logf(Ssum);
-      const int c = cnt[row];
-      float dot = 0.f;
-      for (int k = 0; k < c; ++k) dot += p_sorted[(size_t)row * Kp + k] * zK[(size_t)row * Kp + k];
-      L = ent[row] - dot + lse;
+    const float* pm = part_m + (size_t)row * S;
+    const float* ps = part_s + (size_t)row * S;
+    float m = -INFINITY, s = 0.f;
+    for (int j = lane; j < S; j += 32) lse_merge(m, s, pm[j], ps[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      lse_merge(m, s, m2, s2);
+    }
+    const float lse = m + logf(s);
+    const int c = cnt[row];
+    float dot = 0.f;
+    for (int k = lane; k < c; k += 32) dot += p_sorted[(size_t)row * Kp + k] * zK[(size_t)row * Kp + k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    L = ent[row] - dot + lse;
+    if (lane == 0) {
       lse_out[row] = lse;
       if (loss_rows_out) loss_rows_out[row] = L;
     }
-    sl[lane] = L;
   }
+  if (lane == 0) sl[w] = L;
   __syncthreads();
   if (tid == 0) {
-    double acc = 0.0;
-    for (int i = 0; i < 32; ++i) acc += (double)sl[i];
-    block_sums[blockIdx.x] = acc;
+    double a = 0.0;
+    for (int i = 0; i < 8; ++i) a += (double)sl[i];
+    block_sums[blockIdx.x] = a;
+    __threadfence();
+    last_block = atomicAdd(done, 1u) == gridDim.x - 1;
   }
-}
-
-__global__ void chunk_reduce_kernel(const double* __restrict__ block_sums, int nblocks, double* acc, int first) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  double s = 0.0;
-  for (int i = 0; i < nblocks; ++i) s += block_sums[i];
-  *acc = first ? s : (*acc + s);
+  __syncthreads();
+  // The last block to finish adds the chunk's block sums to the running total,
+  // in block order (lanes take contiguous runs, then a fixed shuffle tree).
+  if (last_block && w == 0) {
+    __threadfence();
+    const int nb = gridDim.x, per = (nb + 31) / 32;
+    double a = 0.0;
+    for (int i = lane * per; i < (lane + 1) * per && i < nb; ++i)
+      a += *reinterpret_cast<volatile double*>(&block_sums[i]);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double b = __shfl_down_sync(0xffffffffu, a, o);
+      if ((lane & (2 * o - 1)) == 0) a += b;
+    }
+    if (lane == 0) {
+      *acc = first ? a : (*acc + a);
+      *done = 0u;  // ready for the next chunk
+    }
+  }
 }
 
 __global__ void finalize_kernel(const double* acc, double inv_T, float* loss) {
@@ -260,17 +281,13 @@ cudaError_t launch_prep(const int32_t* ids, const float* logp, int rows, int K, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_merge(const float* part_m, const float* part_s, int S, int rows, int row_stride,
-                         const float* ent, const float* p_sorted, const float* zK, const int* cnt, int Kp,
-                         float* lse_out, float* loss_rows_out, double* block_sums, cudaStream_t s) {
-  const int nb = (rows + 31) / 32;
-  merge_kernel<<<nb, 256, 0, s>>>(part_m, part_s, S, rows, row_stride, ent, p_sorted, zK, cnt, Kp, lse_out,
-                                  loss_rows_out, block_sums);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_chunk_reduce(const double* block_sums, int nblocks, double* acc, int first, cudaStream_t s) {
-  chunk_reduce_kernel<<<1, 32, 0, s>>>(block_sums, nblocks, acc, first);
+cudaError_t launch_merge(const float* part_m, const float* part_s, int S, int rows, const float* ent,
+                         const float* p_sorted, const float* zK, const int* cnt, int Kp, float* lse_out,
+                         float* loss_rows_out, double* block_sums, unsigned* done, double* acc, int first,
+                         cudaStream_t s) {
+  const int nb = (rows + 7) / 8;
+  merge_kernel<<<nb, 256, 0, s>>>(part_m, part_s, S, rows, ent, p_sorted, zK, cnt, Kp, lse_out, loss_rows_out,
+                                  block_sums, done, acc, first);
   return cudaGetLastError();
 }
 
