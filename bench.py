@@ -370,6 +370,7 @@ def main():
     torch.cuda.synchronize(dev)
     peak_gib = torch.cuda.max_memory_allocated(dev) / 2**30
     ws_gib = ws.numel() / 2**30
+    io_gib = sum(t.numel() * t.element_size() for t in (H, W, ids, logp, lse, loss, dH, dW)) / 2**30
     for _ in range(args.warmup - 1):
         step()
     torch.cuda.synchronize(dev)
@@ -427,6 +428,24 @@ def main():
             kernels[k]["tflops"] = flops_per_launch[k] / (t / n * 1e-3) / 1e12
     gpu_launches = sum(n for n, _ in prof.values())
 
+    # forward and backward separately (same calls, events between them)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for e in evs:
+        e[0].record()
+        _native.check("kd_fused_kl_fwd", L.kd_fused_kl_fwd(
+            H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K, chunk, loss.data_ptr(),
+            lse.data_ptr(), None, ws.data_ptr(), ws.numel(), stream))
+        e[1].record()
+        _native.check("kd_fused_kl_bwd", L.kd_fused_kl_bwd(
+            H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), lse.data_ptr(), T, d, V, K, chunk,
+            1.0 / T, None, dH.data_ptr(), dW.data_ptr(), 0, ws.data_ptr(), ws.numel(), stream))
+        e[2].record()
+    torch.cuda.synchronize(dev)
+    fwd_ms = sorted(e[0].elapsed_time(e[1]) for e in evs)[len(evs) // 2]
+    bwd_ms = sorted(e[1].elapsed_time(e[2]) for e in evs)[len(evs) // 2]
+    phases = {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": 2.0 * T * d * V / (fwd_ms * 1e-3) / 1e12,
+              "bwd_tflops": 6.0 * T * d * V / (bwd_ms * 1e-3) / 1e12, "stat": "median over %d steps" % len(evs)}
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -473,10 +492,12 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "tflops": tflops, "pct_bf16_peak": tflops / peak_tf,
             "pct_bf16_peak_basis": "8*T*d*V flops per step vs bf16_tflops_sustained (%s)" % peaks_src,
-            "peak_gib": peak_gib, "workspace_gib": ws_gib,
+            "peak_gib": peak_gib, "workspace_gib": ws_gib, "io_gib": io_gib, "phases": phases,
             "config": {"workload": describe(args.workload), "parallelism": "replicas" if world > 1 else "1 gpu",
                        "l2": "inputs larger than L2 (W alone is %.0f MB)" % (V * d * 2 / 1e6),
-                       "teacher_cache": "kd_topk_cache of fp32 perturbed-W teacher logits"},
+                       "teacher_cache": "kd_topk_cache of fp32 perturbed-W teacher logits",
+                       "gemm_tiles": "128x256 per CTA" if os.environ.get("KD_GEMM_CTA2") == "0"
+                       else "256x256 per CTA pair (tcgen05 cta_group::2)"},
             "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
             "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "topk_extraction": topk,
         }

@@ -20,6 +20,8 @@ extern "C" {
  *   B: b_mn == 0 -> [N, K] row-major; b_mn == 1 -> [K, N] row-major (bf16).
  *   flags bit 0: add into C instead of overwriting it.
  *   flags bit 1: store C transposed, i.e. C is [N, M] row-major.
+ *   flags bit 2: CTA-pair tiles (256 x 256 per cluster of two CTAs, tcgen05
+ *                cta_group::2); needs b_mn == 0 (else KD_ERR_UNSUPPORTED).
  * Requires K, and M or N for MN-major operands, to be multiples of 8, and
  * C's row length a multiple of 4. `ws` (>= 256 bytes, device) holds the
  * status word and the tile counter. Returns a kd_status value. */

@@ -20,6 +20,13 @@ LOSS_RTOL = 1e-3
 GRAD_RTOL = 1e-2
 
 
+@pytest.fixture(params=["0", "1"], ids=["cta1", "cta2"], autouse=True)
+def gemm_tiles(request, monkeypatch):
+    """Every test runs with one CTA per GEMM tile and with CTA-pair tiles."""
+    monkeypatch.setenv("KD_GEMM_CTA2", request.param)
+    return request.param
+
+
 def frob(a, b):
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)

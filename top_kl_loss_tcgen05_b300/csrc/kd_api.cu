@@ -58,6 +58,15 @@ int num_sms_current() {
   return n;
 }
 
+// GEMM tile shape: 1 = CTA-pair tiles (256 x 256, tcgen05 cta_group::2),
+// 0 = one CTA per 128 x 256 tile. KD_GEMM_CTA2=0/1 overrides the default.
+constexpr int kDefaultCta2 = 1;
+int gemm_cta2() {
+  const char* e = std::getenv("KD_GEMM_CTA2");
+  if (e && (e[0] == '0' || e[0] == '1')) return e[0] - '0';
+  return kDefaultCta2;
+}
+
 // The backward pass groups chunks for its dH/dW GEMM when chunks are small:
 // the fp32 dW read-modify-write (8 V d bytes) then happens once per group
 // instead of once per chunk. The workspace holds the group's dz.
@@ -263,8 +272,10 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
 
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
+  a.cta2 = gemm_cta2();
+  const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
   cudaError_t e = encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V,
-                                (uint64_t)d * 2, kBK, kBNLogits);
+                                (uint64_t)d * 2, kBK, BR);
   if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
   for (int64_t c0 = 0; c0 < T; c0 += chunk) {
     const int rows = (int)((T - c0) < chunk ? (T - c0) : chunk);
@@ -277,7 +288,7 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
                       (uint64_t)d * 2, kBK, kBM);
     if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
     Problem& P = a.pr[0];
-    P.m_blocks = (int)ceil_div(rows, kBM);
+    P.m_blocks = (int)ceil_div(rows, TR);
     P.n_blocks = (int)ceil_div(V, kBNLogits);
     P.k_blocks = (int)ceil_div(d, kBK);
     P.a_mn = 0; P.b_mn = 0;
@@ -330,12 +341,14 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
   GemmArgs az, ag;
   std::memset(&az, 0, sizeof(az));
   std::memset(&ag, 0, sizeof(ag));
+  az.cta2 = ag.cta2 = gemm_cta2();
+  const int TR = gemm_tile_rows(az.cta2), BR = gemm_b_box_rows(az.cta2);
   int* counter = reinterpret_cast<int*>(w + kCounterOffset);
   __nv_bfloat16* hct = reinterpret_cast<__nv_bfloat16*>(w + L.hct);
   cudaError_t e;
   // W: K-major B of the logits GEMM, M-major A of the dH^T GEMM.
   e = encode_map_2d(&az.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2,
-                    kBK, kBNLogits);
+                    kBK, BR);
   if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
   e = encode_map_2d(&ag.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, 64,
                     64);
@@ -364,7 +377,7 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
         return KD_ERR_UNSUPPORTED;
       {
         Problem& P = az.pr[0];
-        P.m_blocks = (int)ceil_div(rows, kBM);
+        P.m_blocks = (int)ceil_div(rows, TR);
         P.n_blocks = (int)ceil_div(V, kBNLogits);
         P.k_blocks = (int)ceil_div(d, kBK);
         P.a_mn = 0; P.b_mn = 0; P.M = rows; P.N = (int)V;
@@ -394,23 +407,23 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
     // dH_g^T = W^T dz^T (problem 0, stored transposed into dH) and
     // dW (+)= dz^T H_g (problem 1), one launch over the group's positions.
     if (encode_map_2d(&ag.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
-                      (uint64_t)L.ldz * 2, kBK, kBNGrad) != cudaSuccess ||
+                      (uint64_t)L.ldz * 2, kBK, BR) != cudaSuccess ||
         encode_map_2d(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dH + g0 * d, (uint64_t)d, (uint64_t)grows,
                       (uint64_t)d * 4, 32, 32) != cudaSuccess ||
         encode_map_2d(&ag.tmA[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
                       (uint64_t)L.ldz * 2, 64, 64) != cudaSuccess ||
         encode_map_2d(&ag.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, hct, (uint64_t)grows, (uint64_t)d,
-                      (uint64_t)L.ldt * 2, kBK, kBNGrad) != cudaSuccess)
+                      (uint64_t)L.ldt * 2, kBK, BR) != cudaSuccess)
       return KD_ERR_UNSUPPORTED;
     {
       Problem& P0 = ag.pr[0];
-      P0.m_blocks = (int)ceil_div(d, kBM);
+      P0.m_blocks = (int)ceil_div(d, TR);
       P0.n_blocks = (int)ceil_div(grows, kBNGrad);
       P0.k_blocks = (int)ceil_div(V, kBK);
       P0.a_mn = 1; P0.b_mn = 0; P0.M = (int)d; P0.N = grows;
       P0.tile_begin = 0; P0.n_fastest = 0; P0.reduce_add = 0; P0.c_trans = 1;
       Problem& P1 = ag.pr[1];
-      P1.m_blocks = (int)ceil_div(V, kBM);
+      P1.m_blocks = (int)ceil_div(V, TR);
       P1.n_blocks = (int)ceil_div(d, kBNGrad);
       P1.k_blocks = (int)ceil_div(grows, kBK);
       P1.a_mn = 1; P1.b_mn = 0; P1.M = (int)V; P1.N = (int)d;
@@ -449,9 +462,10 @@ int kd_test_wait_timeout(int64_t limit_ns, void* ws, void* stream) {
 int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int32_t a_mn,
                  int32_t b_mn, int32_t flags, void* ws, void* stream) {
   if (!A || !B || !C || !ws || M <= 0 || N <= 0 || K <= 0) return KD_ERR_INVALID_ARG;
-  const int reduce_add = flags & 1, c_trans = (flags >> 1) & 1;
+  const int reduce_add = flags & 1, c_trans = (flags >> 1) & 1, cta2 = (flags >> 2) & 1;
   const int64_t ldc = c_trans ? M : N;  // C is [M, N], or [N, M] when stored transposed
   if (K % 8 || (a_mn && M % 8) || (b_mn && N % 8) || ldc % 4) return KD_ERR_UNSUPPORTED;
+  if (cta2 && b_mn) return KD_ERR_UNSUPPORTED;  // the pair tiles read a K-major B only
   if (M >= (1 << 30) || N >= (1 << 30) || K >= (1 << 30)) return KD_ERR_UNSUPPORTED;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
@@ -460,12 +474,14 @@ int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   cudaError_t e1 = a_mn ? encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, M, K, M * 2, 64, 64)
                         : encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, kBK, kBM);
   cudaError_t e2 = b_mn ? encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, N * 2, 64, 64)
-                        : encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, K * 2, kBK, kBNGrad);
+                        : encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, K * 2, kBK,
+                                        gemm_b_box_rows(cta2));
   cudaError_t e3 = c_trans ? encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, M, N, M * 4, 32, 32)
                            : encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, 32);
   if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return KD_ERR_UNSUPPORTED;
+  a.cta2 = cta2;
   Problem& P = a.pr[0];
-  P.m_blocks = (int)ceil_div(M, kBM);
+  P.m_blocks = (int)ceil_div(M, gemm_tile_rows(cta2));
   P.n_blocks = (int)ceil_div(N, kBNGrad);
   P.k_blocks = (int)ceil_div(K, kBK);
   P.a_mn = a_mn ? 1 : 0; P.b_mn = b_mn ? 1 : 0;

@@ -11,14 +11,14 @@
 // These are the operand layouts the tensor core reads at full rate (an
 // N-major B costs 15-28% on B300; an M-major A costs nothing).
 // All run in one persistent, warp-specialised kernel template:
-//   warp 0     TMA producer: one thread takes the next tile from a global
-//              counter (dynamic scheduling), passes its id to the other
-//              roles through a 4-deep shared-memory queue, and streams the
-//              tile's A/B blocks into a ring of shared-memory stages
-//              (128-byte swizzle).
-//   warp 1     MMA issuer: one thread issues tcgen05.mma (M=128, N=BN,
-//              K=16) into one of two TMEM accumulators. tcgen05.commit frees
-//              the smem stage, and then signals the finished accumulator.
+//   warp 0     TMA producer: takes the next tile from a global counter
+//              (dynamic scheduling), passes its id to the other roles through
+//              a 4-deep shared-memory queue, and streams the tile's A/B
+//              blocks into a ring of shared-memory stages (128-byte swizzle).
+//   warp 1     MMA issuer: one thread issues tcgen05.mma (K = 16 per
+//              instruction) into one of two TMEM accumulators.
+//              tcgen05.commit frees the smem stage, and then signals the
+//              finished accumulator.
 //   warps 2-5  epilogue: tcgen05.ld the accumulator (each warp owns 32 TMEM
 //              lanes = 32 rows). While the MMA warp fills the other
 //              accumulator, they run the fused math:
@@ -27,6 +27,15 @@
 //     EPI_DZ    dz = s (exp(z - lse) - p [j in K]) -> bf16 -> TMA store;
 //     EPI_GRAD  fp32 tile -> TMA store or TMA reduce-add (dW += ...),
 //               optionally transposed (dH).
+// Two tile shapes:
+//   C2 = false  one CTA per 128 x 256 tile (tcgen05 cta_group::1, M = 128).
+//   C2 = true   a cluster of two CTAs per 256 x 256 tile (cta_group::2,
+//               M = 256). Each CTA loads its 128 rows of A and its 128-row
+//               half of B; the even CTA issues the MMAs, which read both
+//               CTAs' shared memory and write both CTAs' TMEM (each CTA
+//               holds its own 128 rows of the accumulator). Per SM this
+//               halves the B bytes loaded per MMA and leaves room for a
+//               deeper ring. B must be K-major.
 // The logits tile therefore never leaves the chip in the forward pass. In
 // backward, only the chunk's dz (bf16, c x V) goes to HBM.
 #include <cstdint>
@@ -40,6 +49,8 @@ namespace {
 
 constexpr int EPI_FWD = 0, EPI_DZ = 1, EPI_GRAD = 2;
 constexpr int kThreads = 192;  // 6 warps
+constexpr int BN = kBNLogits;  // N tile (all kernels)
+static_assert(kBNLogits == kBNGrad, "one N tile for all GEMMs");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kStageBytesStaging = 4096;  // one 32-row x 128-byte staging buffer
 constexpr float kLog2e = 1.4426950408889634f;
@@ -51,14 +62,18 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int BN, int NS, int EPI>
+template <int NS, int EPI, bool C2>
 struct Cfg {
-  static constexpr uint32_t A_BYTES = kBM * kBK * 2;
-  static constexpr uint32_t B_BYTES = BN * kBK * 2;
+  static constexpr int TM = C2 ? 2 * kBM : kBM;       // rows of a tile
+  static constexpr int BNL = C2 ? BN / 2 : BN;        // B rows held by one CTA
+  static constexpr uint32_t A_BYTES = kBM * kBK * 2;  // this CTA's A block
+  static constexpr uint32_t B_BYTES = BNL * kBK * 2;  // this CTA's B block
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
+  static constexpr uint32_t TX = C2 ? 2 * STAGE : STAGE;  // bytes that complete one full-barrier phase
   static constexpr uint32_t STG = (EPI == EPI_FWD) ? 0u : 4u * 2u * kStageBytesStaging;
   static constexpr uint32_t BAR_OFF = NS * STAGE + STG;
   static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+  static_assert((2 * NS + 13) * 8 + 24 <= 256, "barrier block");
 };
 
 struct Tile {
@@ -91,30 +106,115 @@ __device__ __forceinline__ int lower_bound(const int* rid, int cnt, int x) {
   return lo;
 }
 
-template <int BN, int NS, int EPI>
+// ------------------------------------------------------------ cluster helpers
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t* local_bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa(smem_u32(local_bar), rank))
+               : "memory");
+}
+__device__ __forceinline__ void st_remote_u32(const volatile int* local, uint32_t rank, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa(smem_u32((const void*)local), rank)), "r"(v)
+               : "memory");
+}
+// Pair TMA load: the bytes land in this CTA's smem and complete on the
+// barrier at cluster address `bar_c` (the even CTA's full barrier).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar_c, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(m), "r"(bar_c), "r"(x), "r"(y)
+      : "memory");
+}
+
+template <bool C2>
+__device__ __forceinline__ void tmem_alloc_x(uint32_t* slot) {
+  if (C2) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    tmem_alloc(slot, kTmemCols);
+    tmem_relinquish();
+  }
+}
+template <bool C2>
+__device__ __forceinline__ void tmem_dealloc_x(uint32_t taddr) {
+  if (C2)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols) : "memory");
+  else
+    tmem_dealloc(taddr, kTmemCols);
+}
+template <bool C2>
+__device__ __forceinline__ void mma_x(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  if (C2)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+  else
+    tc_mma_f16(d, a, b, idesc, accum);
+}
+// Arrives on `bar` once the MMAs issued so far are complete; with C2 also on
+// the barrier at the same offset in the other CTA of the pair.
+template <bool C2>
+__device__ __forceinline__ void commit_x(uint64_t* bar) {
+  if (C2) {
+    const uint16_t mask = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+  } else {
+    tc_commit(bar);
+  }
+}
+
+template <int NS, int EPI, bool C2>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs g) {
-  using C = Cfg<BN, NS, EPI>;
+  using C = Cfg<NS, EPI, C2>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* full = bars;              // [NS] TMA -> MMA
-  uint64_t* empty = bars + NS;        // [NS] MMA -> TMA
-  uint64_t* tfull = bars + 2 * NS;    // [2]  MMA -> epilogue
-  uint64_t* tempty = bars + 2 * NS + 2;  // [2] epilogue -> MMA
-  uint64_t* drain = bars + 2 * NS + 4;   // MMA drain on abort
-  uint64_t* tqf = bars + 2 * NS + 5;     // [4] tile queue: producer -> MMA + epilogue
-  uint64_t* tqe = bars + 2 * NS + 9;     // [4] tile queue: slot free again
+  uint64_t* full = bars;                 // [NS] TMA -> MMA (C2: the even CTA's count both halves)
+  uint64_t* empty = bars + NS;           // [NS] MMA -> TMA
+  uint64_t* tfull = bars + 2 * NS;       // [2]  MMA -> epilogue
+  uint64_t* tempty = bars + 2 * NS + 2;  // [2]  epilogue -> MMA (C2: the even CTA's count both CTAs)
+  uint64_t* drain = bars + 2 * NS + 4;   // all issued MMAs done, before TMEM is released
+  uint64_t* tqf = bars + 2 * NS + 5;     // [4] tile queue: id published
+  uint64_t* tqe = bars + 2 * NS + 9;     // [4] tile queue: slot free again (C2: in the even CTA)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NS + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* tq = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [4] tile ids
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = C2 ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
+  // Readers that release a queue slot: the MMA thread and 4 epilogue warps,
+  // plus (C2) the odd CTA's producer and 4 epilogue warps.
+  constexpr uint32_t kQueueReaders = C2 ? 10u : 5u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], C2 ? 8 : 4); }
     mbar_init(drain, 1);
-    for (int q = 0; q < 4; ++q) { mbar_init(&tqf[q], 1); mbar_init(&tqe[q], 5); }
+    for (int q = 0; q < 4; ++q) { mbar_init(&tqf[q], 1); mbar_init(&tqe[q], kQueueReaders); }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -125,12 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (EPI != EPI_FWD) tma_prefetch_desc(&g.tmC[p]);
     }
   }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
+  if (warp == 1) tmem_alloc_x<C2>(tmem_slot);
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();            // the cluster barrier is .aligned: whole warps arrive together
+  if (C2) cluster_sync();  // barriers of both CTAs initialised before any remote arrive
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -141,36 +240,64 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       uint32_t phase = 0;
       uint32_t issued = 0, ipar = 0;  // per-stage bit: load issued / its phase parity
       bool ok = true;
-      // Tiles are handed out in index order by a global counter: a CTA takes
-      // the next tile when it starts one, so long and short tiles balance.
+      const uint32_t full0_c = C2 ? mapa(smem_u32(full), 0) : 0u;
       for (int j = 0; ok; ++j) {
-        int t = atomicAdd(g.tile_counter, 1);
-        if (t >= g.total_tiles) t = -1;
         const int qs = j & 3;
-        if (!mbar_wait(&tqe[qs], ((uint32_t)(j >> 2) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-        tq[qs] = t;
-        mbar_arrive(&tqf[qs]);
+        const uint32_t qpar = (uint32_t)(j >> 2) & 1u;
+        int t;
+        if (leader) {
+          // Tiles are handed out in index order by a global counter: a CTA
+          // (pair) takes the next tile when it starts one, so long and short
+          // tiles balance.
+          t = atomicAdd(g.tile_counter, 1);
+          if (t >= g.total_tiles) t = -1;
+          if (!mbar_wait<C2>(&tqe[qs], qpar ^ 1u, abort_flag)) { ok = false; break; }
+          tq[qs] = t;
+          if (C2) {
+            st_remote_u32(&tq[qs], 1, (uint32_t)t);
+            mbar_arrive_remote(&tqf[qs], 1);
+          }
+          mbar_arrive(&tqf[qs]);
+        } else {
+          if (!mbar_wait<true>(&tqf[qs], qpar, abort_flag)) { ok = false; break; }
+          t = tq[qs];
+          mbar_arrive_remote(&tqe[qs], 0);
+        }
         if (t < 0) break;
         const Tile tl = decode(g, t);
         const Problem& P = g.pr[tl.prob];
         const CUtensorMap* mA = &g.tmA[tl.prob];
         const CUtensorMap* mB = &g.tmB[tl.prob];
+        const int am = tl.mb * C::TM + (int)rank * kBM;  // this CTA's first A row (M)
+        const int bn = tl.nb * BN + (int)rank * C::BNL;  // this CTA's first B row (N)
         for (int kb = 0; kb < P.k_blocks; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], C::STAGE);
+          if (!mbar_wait<C2>(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t sA = smem_u32(smem + stage * C::STAGE);
           const uint32_t sB = sA + C::A_BYTES;
-          if (!P.a_mn) {
-            tma_load_2d(sA, mA, &full[stage], kb * kBK, tl.mb * kBM);
-          } else {
+          if (C2) {
+            const uint32_t fb = full0_c + (uint32_t)stage * 8u;
+            if (leader) mbar_arrive_expect_tx(&full[stage], C::TX);
+            if (!P.a_mn) {
+              tma_load_2d_pair(sA, mA, fb, kb * kBK, am);
+            } else {
 #pragma unroll
-            for (int q = 0; q < kBM / 64; ++q) tma_load_2d(sA + q * 8192, mA, &full[stage], tl.mb * kBM + q * 64, kb * kBK);
-          }
-          if (!P.b_mn) {
-            tma_load_2d(sB, mB, &full[stage], kb * kBK, tl.nb * BN);
+              for (int q = 0; q < kBM / 64; ++q) tma_load_2d_pair(sA + q * 8192, mA, fb, am + q * 64, kb * kBK);
+            }
+            tma_load_2d_pair(sB, mB, fb, kb * kBK, bn);
           } else {
+            mbar_arrive_expect_tx(&full[stage], C::TX);
+            if (!P.a_mn) {
+              tma_load_2d(sA, mA, &full[stage], kb * kBK, am);
+            } else {
 #pragma unroll
-            for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * 8192, mB, &full[stage], tl.nb * BN + q * 64, kb * kBK);
+              for (int q = 0; q < kBM / 64; ++q) tma_load_2d(sA + q * 8192, mA, &full[stage], am + q * 64, kb * kBK);
+            }
+            if (!P.b_mn) {
+              tma_load_2d(sB, mB, &full[stage], kb * kBK, bn);
+            } else {
+#pragma unroll
+              for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * 8192, mB, &full[stage], bn + q * 64, kb * kBK);
+            }
           }
           issued |= 1u << stage;
           ipar = (ipar & ~(1u << stage)) | (phase << stage);
@@ -181,23 +308,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         set_status(g.status, ST_TIMEOUT);
         *abort_flag = 1;
       }
-      // Never leave the CTA while a TMA load may still write its smem: wait
+      // Never leave while a TMA load may still write shared memory: wait
       // (bounded) until the last load issued into each stage has landed.
       // Nothing else arrives on full[s] afterwards, so the phase it completes
-      // stays the most recent one and the parity wait returns. On the normal
-      // path every load was consumed already and this returns at once.
-      for (int st = 0; st < NS; ++st) {
-        if (!((issued >> st) & 1u)) continue;
-        const uint32_t a = smem_u32(&full[st]);
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(a, (ipar >> st) & 1u)) {
-          if (globaltimer() - t0 > kWaitLimitNs) break;
+      // stays the most recent one and the parity wait returns at once on the
+      // normal path. With C2 the even CTA's barriers also count the odd
+      // CTA's bytes, and the odd CTA leaves only after the final cluster
+      // barrier, i.e. after this wait.
+      if (leader) {
+        for (int st = 0; st < NS; ++st) {
+          if (!((issued >> st) & 1u)) continue;
+          const uint32_t a = smem_u32(&full[st]);
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(a, (ipar >> st) & 1u)) {
+            if (globaltimer() - t0 > kWaitLimitNs) break;
+          }
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -205,46 +336,48 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       bool ok = true;
       for (int j = 0; ok; ++j) {
         const int qs = j & 3;
-        if (!mbar_wait(&tqf[qs], (uint32_t)(j >> 2) & 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait<C2>(&tqf[qs], (uint32_t)(j >> 2) & 1u, abort_flag)) { ok = false; break; }
         const int t = tq[qs];
         mbar_arrive(&tqe[qs]);
         if (t < 0) break;
         const Tile tl = decode(g, t);
         const Problem& P = g.pr[tl.prob];
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait<C2>(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        const uint32_t idesc = idesc_bf16_f32(kBM, BN, P.a_mn, P.b_mn);
+        const int b_mn = C2 ? 0 : P.b_mn;
+        const uint32_t idesc = idesc_bf16_f32(C::TM, BN, P.a_mn, b_mn);
         for (int kb = 0; kb < P.k_blocks; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+          if (!mbar_wait<C2>(&full[stage], phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + stage * C::STAGE);
           const uint32_t sB = sA + C::A_BYTES;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t ad = P.a_mn ? sdesc_sw128(sA + k * 2048, 8192, 1024) : sdesc_sw128(sA + k * 32, 16, 1024);
-            const uint64_t bd = P.b_mn ? sdesc_sw128(sB + k * 2048, 8192, 1024) : sdesc_sw128(sB + k * 32, 16, 1024);
-            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            const uint64_t bd = b_mn ? sdesc_sw128(sB + k * 2048, 8192, 1024) : sdesc_sw128(sB + k * 32, 16, 1024);
+            mma_x<C2>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          tc_commit(&empty[stage]);
+          commit_x<C2>(&empty[stage]);
           if (++stage == NS) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(&tfull[acc]);
+        commit_x<C2>(&tfull[acc]);
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
       if (!ok) {
         set_status(g.status, ST_TIMEOUT);
         *abort_flag = 1;
       }
-      // Let every MMA already issued finish before TMEM is released.
-      tc_commit(drain);
-      {
-        const uint32_t a = smem_u32(drain);
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(a, 0u)) {
-          if (globaltimer() - t0 > kWaitLimitNs) break;
-        }
+      // Let every MMA already issued finish before TMEM is released (with
+      // C2 the arrival reaches the drain barrier of both CTAs).
+      commit_x<C2>(drain);
+    }
+    if (lane == 0) {
+      const uint32_t a = smem_u32(drain);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(a, 0u)) {
+        if (globaltimer() - t0 > kWaitLimitNs) break;
       }
     }
   } else {
@@ -257,17 +390,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint8_t* stg = smem + NS * C::STAGE + (uint32_t)wq * 2u * kStageBytesStaging;
     for (int j = 0;; ++j) {
       const int qs = j & 3;
-      if (!mbar_wait(&tqf[qs], (uint32_t)(j >> 2) & 1u, abort_flag)) ok = false;
+      if (!mbar_wait<C2>(&tqf[qs], (uint32_t)(j >> 2) & 1u, abort_flag)) ok = false;
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       const int t = tq[qs];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tqe[qs]);
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tqe[qs]);
+        else mbar_arrive_remote(&tqe[qs], 0);
+      }
       if (t < 0) break;
       const Tile tl = decode(g, t);
       const Problem& P = g.pr[tl.prob];
-      const int row_l = 32 * wq + lane;
-      const int row = tl.mb * kBM + row_l;
+      const int m0 = tl.mb * C::TM + (int)rank * kBM;  // first tile row held in this CTA's TMEM
+      const int row = m0 + 32 * wq + lane;
       const int n0 = tl.nb * BN;
 
       // Teacher-id cursor of this row for the tile's vocabulary slice.
@@ -283,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
       }
 
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) { ok = false; }
+      if (!mbar_wait<C2>(&tfull[acc], acc_phase, abort_flag)) { ok = false; }
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -299,20 +435,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           float cm = -INFINITY;
           if (lim >= 32) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) cm = fmaxf(cm, u2f(v[j]));
+            for (int jj = 0; jj < 32; ++jj) cm = fmaxf(cm, u2f(v[jj]));
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) if (j < lim) cm = fmaxf(cm, u2f(v[j]));
+            for (int jj = 0; jj < 32; ++jj) if (jj < lim) cm = fmaxf(cm, u2f(v[jj]));
           }
           const float mn = fmaxf(m, cm);
           const float nb2 = -mn * kLog2e;
           float acc_s = 0.f;
           if (lim >= 32) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc_s += ex2(fmaf(u2f(v[j]), kLog2e, nb2));
+            for (int jj = 0; jj < 32; ++jj) acc_s += ex2(fmaf(u2f(v[jj]), kLog2e, nb2));
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) if (j < lim) acc_s += ex2(fmaf(u2f(v[j]), kLog2e, nb2));
+            for (int jj = 0; jj < 32; ++jj) if (jj < lim) acc_s += ex2(fmaf(u2f(v[jj]), kLog2e, nb2));
           }
           s = s * ex2((m - mn) * kLog2e) + acc_s;
           m = mn;
@@ -332,9 +468,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
           u = __reduce_min_sync(0xffffffffu, want);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
         if (row < g.rows) {
           g.part_m[(size_t)row * g.S + tl.nb] = m;
           g.part_s[(size_t)row * g.S + tl.nb] = s;
@@ -343,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const float lse_r = (row < g.rows) ? __ldg(g.lse + row) : 0.f;
         const float sc = g.scale * (g.dscale ? __ldg(g.dscale) : 1.f);
         const float nl = -lse_r * kLog2e;
-        const bool box_live = tl.mb * kBM + 32 * wq < g.rows;
+        const bool box_live = m0 + 32 * wq < g.rows;
         for (int c0 = 0; c0 < nvalid; c0 += 64) {
           const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
           if (nstore >= 2) {
@@ -357,10 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tmem_wait_ld();
             uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float e0 = ex2(fmaf(u2f(v[2 * j]), kLog2e, nl)) * sc;
-              const float e1 = ex2(fmaf(u2f(v[2 * j + 1]), kLog2e, nl)) * sc;
-              pk[j] = pack_bf16x2(e0, e1);
+            for (int jj = 0; jj < 16; ++jj) {
+              const float e0 = ex2(fmaf(u2f(v[2 * jj]), kLog2e, nl)) * sc;
+              const float e1 = ex2(fmaf(u2f(v[2 * jj + 1]), kLog2e, nl)) * sc;
+              pk[jj] = pack_bf16x2(e0, e1);
             }
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
@@ -390,23 +523,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && box_live) {
-            tma_store_2d(&g.tmC[0], sb, n0 + c0, tl.mb * kBM + 32 * wq);
-          }
+          if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, n0 + c0, m0 + 32 * wq);
           if (lane == 0) bulk_commit();
           ++nstore;
           buf ^= 1;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
       } else if (P.c_trans) {
         // C is stored transposed: TMEM lane = column of C, TMEM column = row
         // of C. Each warp stages a 32 x 32 block as [C row][C column] with
         // one 4-byte store per element (conflict-free under the 128-byte
         // swizzle) and stores it with one TMA box.
         const CUtensorMap* mC = &g.tmC[tl.prob];
-        const bool box_live = tl.mb * kBM + 32 * wq < P.M;
+        const bool box_live = m0 + 32 * wq < P.M;
         for (int c0 = 0; c0 < BN && n0 + c0 < P.N; c0 += 32) {
           const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
           if (nstore >= 2) {
@@ -422,19 +550,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && box_live) {
-            if (P.reduce_add) tma_reduce_add_2d(mC, sb, tl.mb * kBM + 32 * wq, n0 + c0);
-            else tma_store_2d(mC, sb, tl.mb * kBM + 32 * wq, n0 + c0);
+            if (P.reduce_add) tma_reduce_add_2d(mC, sb, m0 + 32 * wq, n0 + c0);
+            else tma_store_2d(mC, sb, m0 + 32 * wq, n0 + c0);
           }
           if (lane == 0) bulk_commit();
           ++nstore;
           buf ^= 1;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
       } else {
         const CUtensorMap* mC = &g.tmC[tl.prob];
-        const bool box_live = tl.mb * kBM + 32 * wq < P.M;
+        const bool box_live = m0 + 32 * wq < P.M;
         for (int c0 = 0; c0 < BN && n0 + c0 < P.N; c0 += 32) {
           const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
           if (nstore >= 2) {
@@ -450,16 +575,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && box_live) {
-            if (P.reduce_add) tma_reduce_add_2d(mC, sb, n0 + c0, tl.mb * kBM + 32 * wq);
-            else tma_store_2d(mC, sb, n0 + c0, tl.mb * kBM + 32 * wq);
+            if (P.reduce_add) tma_reduce_add_2d(mC, sb, n0 + c0, m0 + 32 * wq);
+            else tma_store_2d(mC, sb, n0 + c0, m0 + 32 * wq);
           }
           if (lane == 0) bulk_commit();
           ++nstore;
           buf ^= 1;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
+      }
+      // Release the accumulator (C2: the even CTA's barrier counts both CTAs).
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty[acc]);
+        else mbar_arrive_remote(&tempty[acc], 0);
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
@@ -471,38 +600,91 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   }
 
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (C2) cluster_sync();  // neither CTA leaves while the other may still touch its smem or TMEM
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_x<C2>(tmem_base);
   }
 }
 
-template <int BN, int NS, int EPI>
+// Clusters of the pair kernel that fit on the device at once (cached per
+// device and instantiation).
+template <typename KernelT>
+int max_pair_clusters(KernelT k, uint32_t smem) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] > 0) return cache[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cache[dev] = n;
+  return n;
+}
+
+template <int NS, int EPI, bool C2>
 cudaError_t launch(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  using C = Cfg<BN, NS, EPI>;
+  using C = Cfg<NS, EPI, C2>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
-  auto k = gemm_kernel<BN, NS, EPI>;
+  auto k = gemm_kernel<NS, EPI, C2>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  int grid = a.total_tiles < num_sms ? a.total_tiles : num_sms;
-  if (grid < 1) return cudaSuccess;
+  int units = num_sms;  // CTAs, or CTA pairs, resident at once
+  if (C2) {
+    units = max_pair_clusters(k, C::SMEM);
+    if (units <= 0) units = num_sms / 2;
+  }
+  if (a.total_tiles < units) units = a.total_tiles;
+  if (units < 1) return cudaSuccess;
   e = cudaMemsetAsync(a.tile_counter, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, C::SMEM, s>>>(a);
-  return cudaGetLastError();
+  if (!C2) {
+    k<<<units, kThreads, C::SMEM, s>>>(a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(units * 2), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a);
 }
 
 }  // namespace
 
 cudaError_t launch_logits_fwd(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  return launch<kBNLogits, 4, EPI_FWD>(a, num_sms, s);
+  if (a.cta2) return launch<7, EPI_FWD, true>(a, num_sms, s);
+  return launch<4, EPI_FWD, false>(a, num_sms, s);
 }
 cudaError_t launch_logits_dz(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  return launch<kBNLogits, 4, EPI_DZ>(a, num_sms, s);
+  if (a.cta2) return launch<6, EPI_DZ, true>(a, num_sms, s);
+  return launch<4, EPI_DZ, false>(a, num_sms, s);
 }
 cudaError_t launch_grad(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  return launch<kBNGrad, 4, EPI_GRAD>(a, num_sms, s);
+  if (a.cta2) return launch<6, EPI_GRAD, true>(a, num_sms, s);
+  return launch<4, EPI_GRAD, false>(a, num_sms, s);
 }
 
 }  // namespace kd

@@ -51,7 +51,13 @@ struct GemmArgs {
   float scale;            // dz scale
   const float* dscale;    // optional device multiplier of `scale`
   int* status;            // device status word
+  int cta2;               // 1: cluster-pair tiles (256 rows, tcgen05 cta_group::2)
 };
+
+// Rows of one GEMM tile (M extent) for the chosen tile shape; with cta2 the B
+// operand's tensor map box is 128 rows (each CTA of the pair loads half).
+inline int gemm_tile_rows(int cta2) { return cta2 ? 2 * kBM : kBM; }
+inline int gemm_b_box_rows(int cta2) { return cta2 ? kBNLogits / 2 : kBNLogits; }
 
 cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                           uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);

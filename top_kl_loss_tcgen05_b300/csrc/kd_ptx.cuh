@@ -60,14 +60,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Same, with acquire at cluster scope: for phases completed by arrivals
+// (release.cluster) from the other CTA of a cluster.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Waits for the phase with the given parity to complete. Gives up (returns
-// false) when *abort becomes non-zero or after kWaitLimitNs.
+// false) when *abort becomes non-zero or after kWaitLimitNs. CL selects
+// cluster-scope acquire.
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  auto try_once = [&]() { return CL ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
+  if (try_once()) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (try_once()) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
       if (globaltimer() - t0 > kWaitLimitNs) return false;
