@@ -333,6 +333,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-topk", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-fwdbwd", action="store_true", help="skip timing the single-call forward + backward")
     ap.add_argument("--topk-rows", type=int, default=None, help="rows of the top-K workload (default 8192)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -446,6 +447,42 @@ def main():
     phases = {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": 2.0 * T * d * V / (fwd_ms * 1e-3) / 1e12,
               "bwd_tflops": 6.0 * T * d * V / (bwd_ms * 1e-3) / 1e12, "stat": "median over %d steps" % len(evs)}
 
+    # ---- single-call forward + backward (kd_fused_kl_fwdbwd: each chunk's
+    # logits computed once, 6 T d V projection flops). Reported beside the
+    # headline, which is the recompute path (8 T d V).
+    fwdbwd = None
+    if not args.no_fwdbwd:
+        def fb_step():
+            _native.check("kd_fused_kl_fwdbwd", L.kd_fused_kl_fwdbwd(
+                H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K, chunk, 1.0 / T, None,
+                loss.data_ptr(), lse.data_ptr(), None, dH.data_ptr(), dW.data_ptr(), 0, ws.data_ptr(), ws.numel(),
+                stream))
+
+        for _ in range(args.warmup):
+            fb_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        _native.profile_begin()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record()
+        for _ in range(args.steps):
+            fb_step()
+        f1.record()
+        torch.cuda.synchronize(dev)
+        fprof = _native.profile_end()
+        fb_ms = max_over_ranks(f0.elapsed_time(f1), world) / args.steps
+        st = kd.read_device_status(ws)
+        if st != 0:
+            raise RuntimeError("device status %s in kd_fused_kl_fwdbwd" % _native.status_string(st))
+        fb_tot = sum(v[1] for v in fprof.values())
+        fwdbwd = {"value": T * world / (fb_ms * 1e-3), "unit": "tokens/s", "ms_per_step": fb_ms,
+                  "tflops_executed": 6.0 * T * d * V * world / (fb_ms * 1e-3) / 1e12,
+                  "pct_bf16_peak_executed": 6.0 * T * d * V / (fb_ms * 1e-3) / 1e12 / peak_tf,
+                  "flops_basis": "6*T*d*V: the projection is computed once per chunk, no recompute",
+                  "gpu_launches": sum(n for n, _ in fprof.values()),
+                  "kernels": {k: {"launches": n, "ms_per_step": t / args.steps, "share": t / fb_tot if fb_tot else 0.0}
+                              for k, (n, t) in fprof.items()}}
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -499,7 +536,7 @@ def main():
                        "gemm_tiles": "128x256 per CTA" if os.environ.get("KD_GEMM_CTA2") == "0"
                        else "256x256 per CTA pair (tcgen05 cta_group::2)"},
             "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
-            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "topk_extraction": topk,
+            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "topk_extraction": topk, "fused_fwdbwd": fwdbwd,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

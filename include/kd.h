@@ -20,7 +20,8 @@
  *     computed chunk by chunk of positions, so the T x V logit matrix never
  *     exists. The backward pass recomputes each chunk instead of storing it
  *     ([KD-TH] section "กลไก Fused Chunked KL Loss", variant "Fused chunked KL";
- *     [KD-TA] fifth paragraph).
+ *     [KD-TA] fifth paragraph). kd_fused_kl_fwdbwd does both in one call
+ *     without the recompute.
  *
  * What is computed (the oracle's definition). Per position t:
  *   lse_t  = log sum_j exp z_tj over the full vocabulary, z_t = W h_t
@@ -143,7 +144,7 @@ KD_API int kd_topk_cache_noalloc(const void* logits, int32_t dtype, int64_t T, i
  *   Requires d % 8 == 0 (16-byte rows for TMA), 16-byte aligned H and W,
  *   1 <= K <= 4096, 1 <= V < 2^31.
  *   Workspace: kd_fused_kl_workspace_size(d, V, K, chunk) bytes. It does not
- *   depend on T; one workspace serves both calls.
+ *   depend on T; one workspace serves all three calls.
  */
 KD_API size_t kd_fused_kl_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk);
 
@@ -173,6 +174,32 @@ KD_API int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, con
                     int64_t chunk, float grad_scale, const float* grad_scale_dev,
                     float* dH, float* dW, int32_t accumulate_dW,
                     void* ws, size_t ws_bytes, void* stream);
+
+/* Forward and backward in one call, for a loss that ends the graph (its
+ * gradient scale is known before the forward runs). The pages point out
+ * that recomputing each chunk in the backward pass doubles the projection
+ * work ([KD-TA] fifth paragraph). This call computes each chunk's logits
+ * once. It keeps them, until the chunk's lse is known, as
+ * e = exp(z - m_tile) in bf16 inside the O(chunk * V) workspace
+ * (m_tile = the row's maximum over one 256-column vocabulary tile). The
+ * projection costs 6 T d V flops instead of 8, with the same workspace as
+ * kd_fused_kl_fwd/bwd and nothing that grows with T. The teacher side and
+ * the loss are those of [KD-TH] section "กลไก Fused Chunked KL Loss".
+ * Outputs and arguments are those of kd_fused_kl_fwd followed by
+ * kd_fused_kl_bwd (loss, lse and the optional loss_rows; dH overwritten,
+ * dW overwritten or accumulated). The difference is that s = grad_scale
+ * (times *grad_scale_dev) must be known at call time. Results match the
+ * two calls within rounding. dz off the teacher ids is rounded to bf16
+ * twice (e, then dz), so it carries up to about 2^-8 relative error instead
+ * of 2^-9. At the teacher ids, dz is formed from the fp32 logit as in
+ * kd_fused_kl_bwd.
+ * Workspace: kd_fused_kl_workspace_size(d, V, K, chunk), the same as for the
+ * two separate calls. */
+KD_API int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, const float* logp,
+                       int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                       float grad_scale, const float* grad_scale_dev,
+                       float* loss, float* lse, float* loss_rows, float* dH, float* dW,
+                       int32_t accumulate_dW, void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, returns the status word kept in `ws` (KD_OK when no
  * device-side error was recorded) and clears it. Returns KD_ERR_CUDA if the

@@ -25,6 +25,7 @@ __all__ = [
     "fused_kl_workspace",
     "fused_kl_fwd",
     "fused_kl_bwd",
+    "fused_kl_fwdbwd",
     "FusedKL",
     "read_device_status",
     "KDError",
@@ -166,6 +167,38 @@ def fused_kl_bwd(H, W, ids, logp, lse, chunk: int, grad_scale: float, grad_scale
                                       _stream_ptr(dev)),
     )
     return dH, dW
+
+
+def fused_kl_fwdbwd(H, W, ids, logp, chunk: int, grad_scale: float | None = None, grad_scale_dev=None, dH=None,
+                    dW=None, accumulate_dW: bool = False, ws=None, want_rows: bool = False):
+    """Forward and backward in one call, without recomputing the logits:
+    (loss, lse, loss_rows or None, dH, dW). grad_scale defaults to 1/T (the
+    gradient of the mean loss itself)."""
+    T, d, V, K = _check_fused(H, W, ids, logp)
+    dev = H.device
+    if ws is None:
+        ws = fused_kl_workspace(d, V, K, chunk, dev)
+    if grad_scale is None:
+        grad_scale = 1.0 / T
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    rows = torch.empty(T, dtype=torch.float32, device=dev) if want_rows else None
+    if dH is None:
+        dH = torch.empty(T, d, dtype=torch.float32, device=dev)
+    if dW is None:
+        dW = torch.empty(V, d, dtype=torch.float32, device=dev)
+    _need(dH, "dH", torch.float32, dev)
+    _need(dW, "dW", torch.float32, dev)
+    if grad_scale_dev is not None:
+        _need(grad_scale_dev, "grad_scale_dev", torch.float32, dev)
+    check(
+        "kd_fused_kl_fwdbwd",
+        _native.lib().kd_fused_kl_fwdbwd(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K,
+                                         chunk, float(grad_scale), _ptr(grad_scale_dev), loss.data_ptr(),
+                                         lse.data_ptr(), _ptr(rows), dH.data_ptr(), dW.data_ptr(),
+                                         1 if accumulate_dW else 0, ws.data_ptr(), ws.numel(), _stream_ptr(dev)),
+    )
+    return loss, lse, rows, dH, dW
 
 
 class FusedKL(torch.autograd.Function):

@@ -43,6 +43,10 @@ SIGNATURES = {
         ctypes.c_int,
         [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, ctypes.c_float, _P, _P, _P, _I32, _P, _SZ, _P],
     ),
+    "kd_fused_kl_fwdbwd": (
+        ctypes.c_int,
+        [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, ctypes.c_float, _P, _P, _P, _P, _P, _P, _I32, _P, _SZ, _P],
+    ),
     "kd_read_device_status": (ctypes.c_int, [_P, _P]),
     "kd_test_gemm": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32, _P, _P]),
     "kd_test_wait_timeout": (ctypes.c_int, [_I64, _P, _P]),

@@ -72,7 +72,10 @@ int gemm_cta2() {
 // instead of once per chunk. The workspace holds the group's dz.
 int64_t bwd_group(int64_t chunk) { return chunk < 2048 ? 2 : 1; }
 
-// Fused-loss workspace layout (all offsets 256-byte aligned; dz 1024).
+// Fused-loss workspace layout (all offsets 256-byte aligned; dz 1024). One
+// layout serves the forward, the backward and the single-call forward +
+// backward: the per-position arrays hold one group of chunks (G * chunk
+// rows; the separate calls use the first chunk rows of them).
 struct Layout {
   int Kp;
   int64_t G;    // chunks per dH/dW group (backward)
@@ -89,6 +92,7 @@ Layout fused_layout(int64_t d, int64_t V, int K, int64_t chunk) {
   L.ldz = align_up((size_t)V, 64);
   L.G = bwd_group(chunk);
   L.ldt = align_up((size_t)(L.G * chunk), 64);
+  const int64_t prow = L.G * chunk;
   size_t o = kHeader;
   auto take = [&](size_t bytes, size_t al) {
     o = align_up(o, al);
@@ -96,14 +100,14 @@ Layout fused_layout(int64_t d, int64_t V, int K, int64_t chunk) {
     o += bytes;
     return r;
   };
-  L.ids_sorted = take((size_t)chunk * L.Kp * 4, 256);
-  L.p_sorted = take((size_t)chunk * L.Kp * 4, 256);
-  L.cnt = take((size_t)chunk * 4, 256);
-  L.ent = take((size_t)chunk * 4, 256);
-  L.zK = take((size_t)chunk * L.Kp * 4, 256);
-  L.block_sums = take((size_t)ceil_div(chunk, 8) * 8, 256);
-  L.part_m = take((size_t)L.S * chunk * 4, 256);
-  L.part_s = take((size_t)L.S * chunk * 4, 256);
+  L.ids_sorted = take((size_t)prow * L.Kp * 4, 256);
+  L.p_sorted = take((size_t)prow * L.Kp * 4, 256);
+  L.cnt = take((size_t)prow * 4, 256);
+  L.ent = take((size_t)prow * 4, 256);
+  L.zK = take((size_t)prow * L.Kp * 4, 256);
+  L.block_sums = take((size_t)ceil_div(prow, 8) * 8, 256);
+  L.part_m = take((size_t)L.S * prow * 4, 256);
+  L.part_s = take((size_t)L.S * prow * 4, 256);
   L.hct = take((size_t)d * L.ldt * 2, 1024);
   L.dz = take((size_t)(L.G * chunk) * L.ldz * 2, 1024);
   L.total = align_up(o, 256);
@@ -115,11 +119,12 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // ------------------------------------------------------------------ profiling
 // Kernel names reported by kd_profile_end, indexed by KernelId.
 enum KernelId {
-  K_TOPK, K_PREP, K_LOGITS_FWD, K_MERGE, K_FINALIZE, K_LOGITS_DZ, K_TRANSPOSE, K_GRAD, K_TEST, K_COUNT
+  K_TOPK, K_PREP, K_LOGITS_FWD, K_MERGE, K_FINALIZE, K_LOGITS_DZ, K_TRANSPOSE, K_GRAD, K_TEST, K_LOGITS_FWD_STORE,
+  K_DZ_FROM_EXP, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {"topk_cache", "teacher_prep", "logits_fwd_lse_gather", "lse_merge_loss",
                                            "loss_finalize", "logits_dz", "hidden_transpose", "grad_dH_dW",
-                                           "test_gemm"};
+                                           "test_gemm", "logits_fwd_store_exp", "dz_from_exp"};
 struct ProfRec {
   int kid;
   cudaEvent_t a, b;
@@ -193,6 +198,74 @@ cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* 
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+
+namespace {
+
+// dH and dW of one group of positions [g0, g0 + grows) from the group's dz
+// (bf16, [grows, ldz] in the workspace): H_g^T into the workspace, then one
+// GEMM launch with two problems,
+//   dH_g^T = W^T dz^T (stored transposed into dH) and
+//   dW (+)= dz^T H_g.
+// `ag` carries the tensor maps of W (tmA[0]) and dW (tmC[1]) set up once
+// per call.
+int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __nv_bfloat16* dz,
+               __nv_bfloat16* hct, float* dH, int64_t g0, int grows, int64_t d, int64_t V, int reduce_add,
+               int sms, cudaStream_t s) {
+  const int TR = gemm_tile_rows(ag.cta2), BR = gemm_b_box_rows(ag.cta2);
+  cudaError_t e;
+  {
+    ProfScope ps(K_TRANSPOSE, s);
+    e = launch_transpose(Hb + g0 * d, grows, (int)d, hct, (int)L.ldt, s);
+  }
+  if (e != cudaSuccess) return cuda_status(e);
+  if (encode_map_2d(&ag.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
+                    (uint64_t)L.ldz * 2, kBK, BR) != cudaSuccess ||
+      encode_map_2d(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dH + g0 * d, (uint64_t)d, (uint64_t)grows,
+                    (uint64_t)d * 4, 32, 32) != cudaSuccess ||
+      encode_map_2d(&ag.tmA[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
+                    (uint64_t)L.ldz * 2, 64, 64) != cudaSuccess ||
+      encode_map_2d(&ag.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, hct, (uint64_t)grows, (uint64_t)d,
+                    (uint64_t)L.ldt * 2, kBK, BR) != cudaSuccess)
+    return KD_ERR_UNSUPPORTED;
+  Problem& P0 = ag.pr[0];
+  P0.m_blocks = (int)ceil_div(d, TR);
+  P0.n_blocks = (int)ceil_div(grows, kBNGrad);
+  P0.k_blocks = (int)ceil_div(V, kBK);
+  P0.a_mn = 1; P0.b_mn = 0; P0.M = (int)d; P0.N = grows;
+  P0.tile_begin = 0; P0.n_fastest = 0; P0.reduce_add = 0; P0.c_trans = 1;
+  Problem& P1 = ag.pr[1];
+  P1.m_blocks = (int)ceil_div(V, TR);
+  P1.n_blocks = (int)ceil_div(d, kBNGrad);
+  P1.k_blocks = (int)ceil_div(grows, kBK);
+  P1.a_mn = 1; P1.b_mn = 0; P1.M = (int)V; P1.N = (int)d;
+  P1.tile_begin = P0.m_blocks * P0.n_blocks; P1.n_fastest = 1;
+  P1.reduce_add = reduce_add;
+  P1.c_trans = 0;
+  ag.nprob = 2;
+  ag.total_tiles = P1.tile_begin + P1.m_blocks * P1.n_blocks;
+  {
+    ProfScope ps(K_GRAD, s);
+    e = launch_grad(ag, sms, s);
+  }
+  return cuda_status(e);
+}
+
+// Tensor maps of W (M-major A of the dH^T problem) and dW (C of the dW
+// problem), shared by every group of a call.
+int grad_setup(GemmArgs& ag, const void* W, float* dW, int64_t d, int64_t V, int* status, int* counter) {
+  std::memset(&ag, 0, sizeof(ag));
+  ag.cta2 = gemm_cta2();
+  ag.status = status;
+  ag.tile_counter = counter;
+  if (encode_map_2d(&ag.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, 64,
+                    64) != cudaSuccess ||
+      encode_map_2d(&ag.tmC[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, (uint64_t)d, (uint64_t)V, (uint64_t)d * 4, 32,
+                    32) != cudaSuccess)
+    return KD_ERR_UNSUPPORTED;
+  return KD_OK;
+}
+
+}  // namespace
 
 }  // namespace kd
 
@@ -340,8 +413,7 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
 
   GemmArgs az, ag;
   std::memset(&az, 0, sizeof(az));
-  std::memset(&ag, 0, sizeof(ag));
-  az.cta2 = ag.cta2 = gemm_cta2();
+  az.cta2 = gemm_cta2();
   const int TR = gemm_tile_rows(az.cta2), BR = gemm_b_box_rows(az.cta2);
   int* counter = reinterpret_cast<int*>(w + kCounterOffset);
   __nv_bfloat16* hct = reinterpret_cast<__nv_bfloat16*>(w + L.hct);
@@ -350,12 +422,8 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
   e = encode_map_2d(&az.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2,
                     kBK, BR);
   if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
-  e = encode_map_2d(&ag.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, 64,
-                    64);
-  if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
-  e = encode_map_2d(&ag.tmC[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, (uint64_t)d, (uint64_t)V, (uint64_t)d * 4, 32,
-                    32);
-  if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
+  st = grad_setup(ag, W, dW, d, V, status, counter);
+  if (st != KD_OK) return st;
 
   const int64_t gchunk = L.G * chunk;
   for (int64_t g0 = 0; g0 < T; g0 += gchunk) {
@@ -397,51 +465,104 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
       if (e != cudaSuccess) return cuda_status(e);
     }
 
-    // H_g^T [d, grows] (K-major B operand of the dW GEMM).
-    {
-      ProfScope ps(K_TRANSPOSE, s);
-      e = launch_transpose(Hb + g0 * d, grows, (int)d, hct, (int)L.ldt, s);
-    }
-    if (e != cudaSuccess) return cuda_status(e);
-
-    // dH_g^T = W^T dz^T (problem 0, stored transposed into dH) and
-    // dW (+)= dz^T H_g (problem 1), one launch over the group's positions.
-    if (encode_map_2d(&ag.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
-                      (uint64_t)L.ldz * 2, kBK, BR) != cudaSuccess ||
-        encode_map_2d(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dH + g0 * d, (uint64_t)d, (uint64_t)grows,
-                      (uint64_t)d * 4, 32, 32) != cudaSuccess ||
-        encode_map_2d(&ag.tmA[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
-                      (uint64_t)L.ldz * 2, 64, 64) != cudaSuccess ||
-        encode_map_2d(&ag.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, hct, (uint64_t)grows, (uint64_t)d,
-                      (uint64_t)L.ldt * 2, kBK, BR) != cudaSuccess)
-      return KD_ERR_UNSUPPORTED;
-    {
-      Problem& P0 = ag.pr[0];
-      P0.m_blocks = (int)ceil_div(d, TR);
-      P0.n_blocks = (int)ceil_div(grows, kBNGrad);
-      P0.k_blocks = (int)ceil_div(V, kBK);
-      P0.a_mn = 1; P0.b_mn = 0; P0.M = (int)d; P0.N = grows;
-      P0.tile_begin = 0; P0.n_fastest = 0; P0.reduce_add = 0; P0.c_trans = 1;
-      Problem& P1 = ag.pr[1];
-      P1.m_blocks = (int)ceil_div(V, TR);
-      P1.n_blocks = (int)ceil_div(d, kBNGrad);
-      P1.k_blocks = (int)ceil_div(grows, kBK);
-      P1.a_mn = 1; P1.b_mn = 0; P1.M = (int)V; P1.N = (int)d;
-      P1.tile_begin = P0.m_blocks * P0.n_blocks; P1.n_fastest = 1;
-      P1.reduce_add = (accumulate_dW || g0 > 0) ? 1 : 0;
-      P1.c_trans = 0;
-      ag.nprob = 2;
-      ag.total_tiles = P1.tile_begin + P1.m_blocks * P1.n_blocks;
-      ag.status = status;
-      ag.tile_counter = counter;
-    }
-    {
-      ProfScope ps(K_GRAD, s);
-      e = launch_grad(ag, sms, s);
-    }
-    if (e != cudaSuccess) return cuda_status(e);
+    st = grad_group(ag, L, Hb, dz, hct, dH, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms, s);
+    if (st != KD_OK) return st;
   }
   return KD_OK;
+}
+
+int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
+                       int64_t V, int32_t K, int64_t chunk, float grad_scale, const float* grad_scale_dev,
+                       float* loss, float* lse, float* loss_rows, float* dH, float* dW, int32_t accumulate_dW,
+                       void* ws, size_t ws_bytes, void* stream) {
+  int st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, ws, ws_bytes);
+  if (st != KD_OK) return st;
+  if (!loss || !lse || !dH || !dW) return KD_ERR_INVALID_ARG;
+  if (!aligned(dH, 16) || !aligned(dW, 16)) return KD_ERR_UNSUPPORTED;
+  const int sms = num_sms_current();
+  if (sms <= 0) return KD_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = fused_layout(d, V, K, chunk);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* status = reinterpret_cast<int*>(w);
+  int* counter = reinterpret_cast<int*>(w + kCounterOffset);
+  double* acc = reinterpret_cast<double*>(w + kAccOffset);
+  unsigned* done = reinterpret_cast<unsigned*>(w + kDoneOffset);
+  int* ids_sorted = reinterpret_cast<int*>(w + L.ids_sorted);
+  float* p_sorted = reinterpret_cast<float*>(w + L.p_sorted);
+  int* cnt = reinterpret_cast<int*>(w + L.cnt);
+  float* ent = reinterpret_cast<float*>(w + L.ent);
+  float* zK = reinterpret_cast<float*>(w + L.zK);
+  double* bsum = reinterpret_cast<double*>(w + L.block_sums);
+  float* part_m = reinterpret_cast<float*>(w + L.part_m);
+  float* part_s = reinterpret_cast<float*>(w + L.part_s);
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(w + L.dz);
+  __nv_bfloat16* hct = reinterpret_cast<__nv_bfloat16*>(w + L.hct);
+  const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
+  cudaError_t e = cudaMemsetAsync(done, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return cuda_status(e);
+
+  GemmArgs a, ag;
+  std::memset(&a, 0, sizeof(a));
+  a.cta2 = gemm_cta2();
+  const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
+  if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
+                    BR) != cudaSuccess)
+    return KD_ERR_UNSUPPORTED;
+  st = grad_setup(ag, W, dW, d, V, status, counter);
+  if (st != KD_OK) return st;
+
+  // One group of G chunks at a time: the group's logits are computed once,
+  // and kept only as e = exp(z - m_tile) (bf16, in the dz buffer) until the
+  // group's lse is known.
+  const int64_t gchunk = L.G * chunk;
+  for (int64_t g0 = 0; g0 < T; g0 += gchunk) {
+    const int grows = (int)((T - g0) < gchunk ? (T - g0) : gchunk);
+    {
+      ProfScope ps(K_PREP, s);
+      e = launch_prep(ids + g0 * K, logp + g0 * K, grows, K, (int)V, L.Kp, ids_sorted, p_sorted, cnt, ent, status, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    if (encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + g0 * d, (uint64_t)d, (uint64_t)grows,
+                      (uint64_t)d * 2, kBK, kBM) != cudaSuccess ||
+        encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
+                      (uint64_t)L.ldz * 2, 64, 32) != cudaSuccess)
+      return KD_ERR_UNSUPPORTED;
+    Problem& P = a.pr[0];
+    P.m_blocks = (int)ceil_div(grows, TR);
+    P.n_blocks = (int)ceil_div(V, kBNLogits);
+    P.k_blocks = (int)ceil_div(d, kBK);
+    P.a_mn = 0; P.b_mn = 0; P.M = grows; P.N = (int)V;
+    P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
+    a.nprob = 1;
+    a.total_tiles = P.m_blocks * P.n_blocks;
+    a.rows = grows; a.row_stride = (int)gchunk; a.S = (int)L.S; a.V = (int)V; a.Kp = L.Kp;
+    a.ids_sorted = ids_sorted; a.p_sorted = p_sorted; a.cnt = cnt;
+    a.zK = zK; a.part_m = part_m; a.part_s = part_s;
+    a.status = status;
+    a.tile_counter = counter;
+    {
+      ProfScope ps(K_LOGITS_FWD_STORE, s);
+      e = launch_logits_fwd_store(a, sms, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    {
+      ProfScope ps(K_MERGE, s);
+      e = launch_merge(part_m, part_s, (int)L.S, grows, ent, p_sorted, zK, cnt, L.Kp, lse + g0,
+                       loss_rows ? loss_rows + g0 : nullptr, bsum, done, acc, g0 == 0, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    {
+      ProfScope ps(K_DZ_FROM_EXP, s);
+      e = launch_dz_from_exp(dz, L.ldz, (int)V, (int)L.S, grows, part_m, lse + g0, ids_sorted, p_sorted, zK, cnt,
+                             L.Kp, grad_scale, grad_scale_dev, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    st = grad_group(ag, L, Hb, dz, hct, dH, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms, s);
+    if (st != KD_OK) return st;
+  }
+  ProfScope ps(K_FINALIZE, s);
+  return cuda_status(launch_finalize(acc, 1.0 / (double)T, loss, s));
 }
 
 int kd_read_device_status(void* ws, void* stream) {

@@ -26,7 +26,11 @@
 //               slice, and the logits at the teacher ids that fall in it;
 //     EPI_DZ    dz = s (exp(z - lse) - p [j in K]) -> bf16 -> TMA store;
 //     EPI_GRAD  fp32 tile -> TMA store or TMA reduce-add (dW += ...),
-//               optionally transposed (dH).
+//               optionally transposed (dH);
+//     EPI_FWDST the EPI_FWD results, with the tile's maximum m as the
+//               reference, plus e = exp(z - m) -> bf16 -> TMA store, from
+//               which the single-call forward + backward forms dz without
+//               recomputing the logits.
 // Two tile shapes:
 //   C2 = false  one CTA per 128 x 256 tile (tcgen05 cta_group::1, M = 128).
 //   C2 = true   a cluster of two CTAs per 256 x 256 tile (cta_group::2,
@@ -47,20 +51,14 @@
 namespace kd {
 namespace {
 
-constexpr int EPI_FWD = 0, EPI_DZ = 1, EPI_GRAD = 2;
+constexpr int EPI_FWD = 0, EPI_DZ = 1, EPI_GRAD = 2, EPI_FWDST = 3;
 constexpr int kThreads = 192;  // 6 warps
 constexpr int BN = kBNLogits;  // N tile (all kernels)
 static_assert(kBNLogits == kBNGrad, "one N tile for all GEMMs");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kStageBytesStaging = 4096;  // one 32-row x 128-byte staging buffer
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 template <int NS, int EPI, bool C2>
 struct Cfg {
@@ -425,7 +423,81 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(acc * BN);
 
-      if (EPI == EPI_FWD) {
+      if (EPI == EPI_FWDST) {
+        // Pass 1: the row's maximum over the tile's valid columns.
+        float m = -INFINITY;
+        for (int c0 = 0; c0 < nvalid; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c0, v);
+          tmem_wait_ld();
+          const int lim = nvalid - c0;
+          if (lim >= 32) {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) m = fmaxf(m, u2f(v[jj]));
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) if (jj < lim) m = fmaxf(m, u2f(v[jj]));
+          }
+        }
+        // Pass 2: e = exp(z - m) summed in fp32 and stored as bf16, 64
+        // columns per TMA box (columns past V are clipped by the store).
+        const float nm = -m * kLog2e;
+        float s = 0.f;
+        const bool box_live = m0 + 32 * wq < g.rows;
+        for (int c0 = 0; c0 < nvalid; c0 += 64) {
+          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
+          if (nstore >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c0 + 32 * h, v);
+            tmem_wait_ld();
+            const int lim = nvalid - c0 - 32 * h;
+            uint32_t pk[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const float e0 = ex2(fmaf(u2f(v[2 * jj]), kLog2e, nm));
+              const float e1 = ex2(fmaf(u2f(v[2 * jj + 1]), kLog2e, nm));
+              if (2 * jj < lim) s += e0;
+              if (2 * jj + 1 < lim) s += e1;
+              pk[jj] = pack_bf16x2(e0, e1);
+            }
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const int q = h * 4 + qq;
+              st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4), pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2],
+                           pk[4 * qq + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, n0 + c0, m0 + 32 * wq);
+          if (lane == 0) bulk_commit();
+          ++nstore;
+          buf ^= 1;
+        }
+        // Logits at the teacher ids inside the tile (fp32, from TMEM).
+        const uint32_t hiend = (uint32_t)(n0 + nvalid);
+        uint32_t want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
+        uint32_t u = __reduce_min_sync(0xffffffffu, want);
+        while (u != kNone) {
+          const uint32_t val = tmem_ld1(taddr + (u - (uint32_t)n0));
+          tmem_wait_ld();
+          if (want == u) {
+            g.zK[(size_t)row * g.Kp + k] = u2f(val);
+            ++k;
+            want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
+          }
+          u = __reduce_min_sync(0xffffffffu, want);
+        }
+        if (row < g.rows) {
+          g.part_m[(size_t)row * g.S + tl.nb] = m;
+          g.part_s[(size_t)row * g.S + tl.nb] = s;
+        }
+      } else if (EPI == EPI_FWD) {
         float m = -INFINITY, s = 0.f;
         for (int c0 = 0; c0 < nvalid; c0 += 32) {
           uint32_t v[32];
@@ -681,6 +753,10 @@ cudaError_t launch_logits_fwd(const GemmArgs& a, int num_sms, cudaStream_t s) {
 cudaError_t launch_logits_dz(const GemmArgs& a, int num_sms, cudaStream_t s) {
   if (a.cta2) return launch<6, EPI_DZ, true>(a, num_sms, s);
   return launch<4, EPI_DZ, false>(a, num_sms, s);
+}
+cudaError_t launch_logits_fwd_store(const GemmArgs& a, int num_sms, cudaStream_t s) {
+  if (a.cta2) return launch<6, EPI_FWDST, true>(a, num_sms, s);
+  return launch<4, EPI_FWDST, false>(a, num_sms, s);
 }
 cudaError_t launch_grad(const GemmArgs& a, int num_sms, cudaStream_t s) {
   if (a.cta2) return launch<6, EPI_GRAD, true>(a, num_sms, s);

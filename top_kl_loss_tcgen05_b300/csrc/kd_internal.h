@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace kd {
@@ -65,6 +66,7 @@ cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* 
 // Launchers (kd_gemm.cu).
 cudaError_t launch_logits_fwd(const GemmArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_logits_dz(const GemmArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_logits_fwd_store(const GemmArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_grad(const GemmArgs& a, int num_sms, cudaStream_t s);
 
 // Small kernels (kd_loss_aux.cu).
@@ -74,6 +76,9 @@ cudaError_t launch_merge(const float* part_m, const float* part_s, int S, int ro
                          const float* p_sorted, const float* zK, const int* cnt, int Kp, float* lse_out,
                          float* loss_rows_out, double* block_sums, unsigned* done, double* acc, int first,
                          cudaStream_t s);
+cudaError_t launch_dz_from_exp(__nv_bfloat16* E, int64_t ldz, int V, int S, int rows, const float* part_m,
+                               const float* lse, const int* ids_sorted, const float* p_sorted, const float* zK,
+                               const int* cnt, int Kp, float scale, const float* dscale, cudaStream_t s);
 cudaError_t launch_finalize(const double* acc, double inv_T, float* loss, cudaStream_t s);
 cudaError_t launch_transpose(const void* src, int rows, int cols, void* dst, int ld_dst, cudaStream_t s);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s);

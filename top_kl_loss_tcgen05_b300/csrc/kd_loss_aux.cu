@@ -10,6 +10,11 @@
 //          L_t = sum p log p - sum_k p_k z_id_k + lse_t; a per-block sum.
 //          The last block of a chunk adds the chunk's block sums to the
 //          running fp64 total in a fixed order; finally loss = total / T.
+//  dz      (single-call forward + backward) dz = s (q - p 1[j in K]) from
+//          the forward GEMM's stored e = exp(z - m_tile) in bf16:
+//          q_j = e_j exp(m_tile - lse) off the K ids; at the K ids q comes
+//          from the fp32 logit the forward gathered, so q - p is formed
+//          from unrounded values exactly as in the recompute path.
 // All reductions run in a fixed order, so the loss is bitwise reproducible.
 // Definition: "ทำให้ Knowledge Distillation มีประสิทธิภาพ..." (ai-thai.com),
 // section "กลไก Fused Chunked KL Loss". The KL direction, the
@@ -252,7 +257,66 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns, int* status) {
   }
 }
 
+// One block per position, streaming its row of e in 16-byte vectors and
+// rewriting it in place as dz (bf16), then the row's K entries.
+constexpr int kDzThreads = 256;
+
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t u, float f) {
+  const float lo = __uint_as_float(u << 16) * f;
+  const float hi = __uint_as_float(u & 0xFFFF0000u) * f;
+  return pack_bf16x2(lo, hi);
+}
+
+__global__ void __launch_bounds__(kDzThreads) dz_from_exp_kernel(uint16_t* __restrict__ E, int64_t ldz, int V, int S,
+                                                                const float* __restrict__ part_m,
+                                                                const float* __restrict__ lse,
+                                                                const int* __restrict__ ids_sorted,
+                                                                const float* __restrict__ p_sorted,
+                                                                const float* __restrict__ zK,
+                                                                const int* __restrict__ cnt, int Kp, float scale,
+                                                                const float* __restrict__ dscale) {
+  const int r = blockIdx.x;
+  const float sc = scale * (dscale ? __ldg(dscale) : 1.f);
+  const float l2 = __ldg(lse + r) * kLog2e;
+  uint16_t* row = E + (size_t)r * ldz;
+  const float* pm = part_m + (size_t)r * S;
+  uint4* rv = reinterpret_cast<uint4*>(row);
+  const int nvec = V >> 3;  // 8 columns per vector, never straddling a 256-column tile
+  for (int v = threadIdx.x; v < nvec; v += kDzThreads) {
+    const float f = sc * ex2(fmaf(__ldg(pm + ((v << 3) / kBNLogits)), kLog2e, -l2));
+    uint4 x = rv[v];
+    x.x = scale_bf16x2(x.x, f);
+    x.y = scale_bf16x2(x.y, f);
+    x.z = scale_bf16x2(x.z, f);
+    x.w = scale_bf16x2(x.w, f);
+    rv[v] = x;
+  }
+  for (int j = (nvec << 3) + threadIdx.x; j < V; j += kDzThreads) {
+    const float f = sc * ex2(fmaf(__ldg(pm + j / kBNLogits), kLog2e, -l2));
+    const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float((uint32_t)row[j] << 16) * f);
+    row[j] = *reinterpret_cast<const uint16_t*>(&h);
+  }
+  __syncthreads();  // the row's bulk writes land before its K entries are overwritten
+  const int c = __ldg(cnt + r);
+  for (int k = threadIdx.x; k < c; k += kDzThreads) {
+    const size_t o = (size_t)r * Kp + k;
+    const int j = __ldg(ids_sorted + o);
+    const float q = ex2(fmaf(__ldg(zK + o), kLog2e, -l2));
+    const __nv_bfloat16 h = __float2bfloat16_rn(sc * (q - __ldg(p_sorted + o)));
+    row[j] = *reinterpret_cast<const uint16_t*>(&h);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_dz_from_exp(__nv_bfloat16* E, int64_t ldz, int V, int S, int rows, const float* part_m,
+                               const float* lse, const int* ids_sorted, const float* p_sorted, const float* zK,
+                               const int* cnt, int Kp, float scale, const float* dscale, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  dz_from_exp_kernel<<<rows, kDzThreads, 0, s>>>(reinterpret_cast<uint16_t*>(E), ldz, V, S, part_m, lse, ids_sorted,
+                                                p_sorted, zK, cnt, Kp, scale, dscale);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s) {
   wait_timeout_kernel<<<1, 32, 0, s>>>(limit_ns, status);

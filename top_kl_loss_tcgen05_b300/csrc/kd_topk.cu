@@ -39,13 +39,7 @@ constexpr int kCandCap = 2048;   // candidate buffer entries (fast path)
 constexpr int kFastMaxK = 1024;  // larger K goes to the exact path
 constexpr int kBatch = 8;        // 16-byte loads per thread in flight in pass 1
 constexpr int kSlots = 16;       // per-thread batch-maximum slots kept for pass 2
-constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // Order-preserving map float -> uint32 (larger float -> larger key), with
 // -0.0 mapped to the key of +0.0.
