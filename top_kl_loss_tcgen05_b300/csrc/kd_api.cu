@@ -4,11 +4,14 @@
 // The chunk loop is the structure of the "Fused chunked KL" variant ("ทำให้
 // Knowledge Distillation มีประสิทธิภาพ..." (ai-thai.com), section "กลไก Fused
 // Chunked KL Loss"; "Multiverse Computing сократила видеопамять..."
-// (iitog.ru), fourth paragraph). Positions are processed one chunk at a time:
+// (iitog.ru), fourth paragraph). Positions are processed one group of G
+// chunks at a time (G = 2 below 2048 positions per chunk, else 1):
 //   forward : prep -> logits GEMM with (max, sum, gather) epilogue -> merge
 //   backward: prep -> logits GEMM recompute with dz epilogue -> dH + dW GEMMs
-// The only per-chunk buffers (in the caller's workspace) are O(chunk * V):
-// the bf16 dz of one chunk and the per-tile partials. Nothing grows with T
+//   fwdbwd  : prep -> logits GEMM storing exp(z - m_tile) -> merge -> dz pass
+//             -> dH + dW GEMMs
+// The only per-group buffers (in the caller's workspace) are O(G * chunk * V):
+// the bf16 dz of one group and the per-tile partials. Nothing grows with T
 // apart from the caller's own inputs and outputs.
 #include <cstdint>
 #include <cstdio>
@@ -350,8 +353,12 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
   cudaError_t e = encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V,
                                 (uint64_t)d * 2, kBK, BR);
   if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
-  for (int64_t c0 = 0; c0 < T; c0 += chunk) {
-    const int rows = (int)((T - c0) < chunk ? (T - c0) : chunk);
+  // Positions go through in groups of G chunks (one GEMM launch per group:
+  // more tiles per launch, fewer launches; the group is the unit the
+  // workspace is sized for).
+  const int64_t gchunk = L.G * chunk;
+  for (int64_t c0 = 0; c0 < T; c0 += gchunk) {
+    const int rows = (int)((T - c0) < gchunk ? (T - c0) : gchunk);
     {
       ProfScope ps(K_PREP, s);
       e = launch_prep(ids + c0 * K, logp + c0 * K, rows, K, (int)V, L.Kp, ids_sorted, p_sorted, cnt, ent, status, s);
@@ -369,7 +376,7 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
     P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0;
     a.nprob = 1;
     a.total_tiles = P.m_blocks * P.n_blocks;
-    a.rows = rows; a.row_stride = (int)chunk; a.S = (int)L.S; a.V = (int)V; a.Kp = L.Kp;
+    a.rows = rows; a.row_stride = (int)gchunk; a.S = (int)L.S; a.V = (int)V; a.Kp = L.Kp;
     a.ids_sorted = ids_sorted; a.p_sorted = p_sorted; a.cnt = cnt;
     a.zK = zK; a.part_m = part_m; a.part_s = part_s;
     a.status = status;
@@ -425,46 +432,42 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
   st = grad_setup(ag, W, dW, d, V, status, counter);
   if (st != KD_OK) return st;
 
+  // One group of G chunks at a time: prep, the recompute GEMM writing the
+  // group's dz, then dH and dW of the group.
   const int64_t gchunk = L.G * chunk;
   for (int64_t g0 = 0; g0 < T; g0 += gchunk) {
     const int grows = (int)((T - g0) < gchunk ? (T - g0) : gchunk);
-    for (int64_t c0 = g0; c0 < g0 + grows; c0 += chunk) {
-      const int rows = (int)((T - c0) < chunk ? (T - c0) : chunk);
-      {
-        ProfScope ps(K_PREP, s);
-        e = launch_prep(ids + c0 * K, logp + c0 * K, rows, K, (int)V, L.Kp, ids_sorted, p_sorted, cnt, ent, status,
-                        s);
-      }
-      if (e != cudaSuccess) return cuda_status(e);
-
-      // Recompute the chunk's logits; the epilogue writes its rows of dz (bf16).
-      if (encode_map_2d(&az.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + c0 * d, (uint64_t)d, (uint64_t)rows,
-                        (uint64_t)d * 2, kBK, kBM) != cudaSuccess ||
-          encode_map_2d(&az.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz + (c0 - g0) * L.ldz, (uint64_t)V,
-                        (uint64_t)rows, (uint64_t)L.ldz * 2, 64, 32) != cudaSuccess)
-        return KD_ERR_UNSUPPORTED;
-      {
-        Problem& P = az.pr[0];
-        P.m_blocks = (int)ceil_div(rows, TR);
-        P.n_blocks = (int)ceil_div(V, kBNLogits);
-        P.k_blocks = (int)ceil_div(d, kBK);
-        P.a_mn = 0; P.b_mn = 0; P.M = rows; P.N = (int)V;
-        P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
-        az.nprob = 1;
-        az.total_tiles = P.m_blocks * P.n_blocks;
-        az.rows = rows; az.row_stride = (int)chunk; az.V = (int)V; az.Kp = L.Kp;
-        az.ids_sorted = ids_sorted; az.p_sorted = p_sorted; az.cnt = cnt;
-        az.lse = lse + c0; az.scale = grad_scale; az.dscale = grad_scale_dev;
-        az.status = status;
-        az.tile_counter = counter;
-      }
-      {
-        ProfScope ps(K_LOGITS_DZ, s);
-        e = launch_logits_dz(az, sms, s);
-      }
-      if (e != cudaSuccess) return cuda_status(e);
+    {
+      ProfScope ps(K_PREP, s);
+      e = launch_prep(ids + g0 * K, logp + g0 * K, grows, K, (int)V, L.Kp, ids_sorted, p_sorted, cnt, ent, status, s);
     }
-
+    if (e != cudaSuccess) return cuda_status(e);
+    // Recompute the group's logits; the epilogue writes dz (bf16).
+    if (encode_map_2d(&az.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + g0 * d, (uint64_t)d, (uint64_t)grows,
+                      (uint64_t)d * 2, kBK, kBM) != cudaSuccess ||
+        encode_map_2d(&az.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
+                      (uint64_t)L.ldz * 2, 64, 32) != cudaSuccess)
+      return KD_ERR_UNSUPPORTED;
+    {
+      Problem& P = az.pr[0];
+      P.m_blocks = (int)ceil_div(grows, TR);
+      P.n_blocks = (int)ceil_div(V, kBNLogits);
+      P.k_blocks = (int)ceil_div(d, kBK);
+      P.a_mn = 0; P.b_mn = 0; P.M = grows; P.N = (int)V;
+      P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
+      az.nprob = 1;
+      az.total_tiles = P.m_blocks * P.n_blocks;
+      az.rows = grows; az.row_stride = (int)gchunk; az.V = (int)V; az.Kp = L.Kp;
+      az.ids_sorted = ids_sorted; az.p_sorted = p_sorted; az.cnt = cnt;
+      az.lse = lse + g0; az.scale = grad_scale; az.dscale = grad_scale_dev;
+      az.status = status;
+      az.tile_counter = counter;
+    }
+    {
+      ProfScope ps(K_LOGITS_DZ, s);
+      e = launch_logits_dz(az, sms, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
     st = grad_group(ag, L, Hb, dz, hct, dH, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms, s);
     if (st != KD_OK) return st;
   }

@@ -143,19 +143,144 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* __res
   if (tid == 0) cnt[r] = base_out;
 }
 
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
-  if (m2 == -INFINITY) return;
-  if (m == -INFINITY) { m = m2; s = s2; return; }
-  const float mm = fmaxf(m, m2);
-  s = s * expf(m - mm) + s2 * expf(m2 - mm);
-  m = mm;
+// The same teacher prep with one warp per row, for K <= 128 (the cache
+// sizes of the method: K = 100). Each lane holds 4 of the row's entries;
+// the (id, slot) keys are sorted by a 128-element bitonic network in
+// registers and shuffles (sort position = 4 * lane + q), so no block-wide
+// barrier is involved and a launch takes about one row's latency.
+constexpr int kPrepWarpK = 128;
+constexpr int kPrepWarpRows = 8;  // rows (warps) per block
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
 }
 
-// One warp per position, 8 positions per block. Each lane merges every 32nd
+__global__ void __launch_bounds__(32 * kPrepWarpRows) prep_warp_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ logp, int rows, int K, int V, int Kp,
+    int* __restrict__ ids_sorted, float* __restrict__ p_sorted, int* __restrict__ cnt, float* __restrict__ ent,
+    int* status) {
+  __shared__ uint64_t skeys[kPrepWarpRows][kPrepWarpK];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kPrepWarpRows + w;
+  if (r >= rows) return;  // whole warps only; nothing below synchronises the block
+  const int32_t* rid = ids + (size_t)r * K;
+  const float* rl = logp + (size_t)r * K;
+
+  float lv[4];
+  uint64_t key[4];
+  bool bad = false;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = lane + 32 * q;  // original slot of this register
+    lv[q] = -INFINITY;
+    key[q] = kDropKey;
+    if (i < K) {
+      lv[q] = __ldg(rl + i);
+      const int id = __ldg(rid + i);
+      if (id < 0 || id >= V) bad = true;
+      else key[q] = ((uint64_t)(uint32_t)id << 32) | (uint32_t)i;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, ST_BAD_ID);
+
+  // Teacher renormalised over its K entries, and sum p log p.
+  float mx = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) mx = fmaxf(mx, lv[q]);
+  mx = warp_max(mx);
+  float se = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) if (lane + 32 * q < K) se += expf(lv[q] - mx);
+  se = warp_sum(se);
+  const float lse_k = mx + logf(se);
+  float e = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (lane + 32 * q < K) {
+      const float lp = lv[q] - lse_k;
+      e += expf(lp) * lp;
+    }
+  }
+  e = warp_sum(e);
+  if (lane == 0) ent[r] = e;
+
+  // Ascending bitonic sort of the 128 keys; position 4 * lane + q.
+#pragma unroll
+  for (int k = 2; k <= kPrepWarpK; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= 4) {
+        const int lj = j >> 2;
+        const bool lower = (lane & lj) == 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint64_t o = __shfl_xor_sync(0xffffffffu, key[q], lj);
+          const bool up = (((lane << 2) | q) & k) == 0;
+          const uint64_t lo = key[q] < o ? key[q] : o, hi = key[q] < o ? o : key[q];
+          key[q] = (lower == up) ? lo : hi;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q & j) continue;
+          const int p = q | j;
+          const bool up = (((lane << 2) | q) & k) == 0;
+          const uint64_t a = key[q], b = key[p];
+          if (up ? (a > b) : (a < b)) { key[q] = b; key[p] = a; }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) skeys[w][(lane << 2) | q] = key[q];
+  __syncwarp();
+
+  // One output entry per distinct id (a run of equal ids), with the summed
+  // probability (the scatter-add of duplicates); slots in id order.
+  bool head[4];
+  int hc = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int pos = (lane << 2) | q;
+    const uint64_t kq = key[q];
+    head[q] = kq != kDropKey &&
+              (pos == 0 || skeys[w][pos - 1] == kDropKey || (uint32_t)(skeys[w][pos - 1] >> 32) != (uint32_t)(kq >> 32));
+    hc += head[q] ? 1 : 0;
+  }
+  int incl = hc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  int slot = incl - hc;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (!head[q]) continue;
+    const int pos = (lane << 2) | q;
+    const uint32_t id = (uint32_t)(key[q] >> 32);
+    float ps = 0.f;
+    for (int j = pos; j < kPrepWarpK && skeys[w][j] != kDropKey && (uint32_t)(skeys[w][j] >> 32) == id; ++j)
+      ps += expf(__ldg(rl + (uint32_t)skeys[w][j]) - lse_k);
+    ids_sorted[(size_t)r * Kp + slot] = (int)id;
+    p_sorted[(size_t)r * Kp + slot] = ps;
+    ++slot;
+  }
+  if (lane == 31) cnt[r] = incl;
+}
+
+// One warp per position, 8 positions per block. Each lane takes every 32nd
 // vocabulary-tile partial of the row (a coalesced read of the row's [S]
-// partials), then the lanes are combined by an xor-shuffle tree. The merge
-// is commutative, so every lane ends with the same value. The block sum of
-// its 8 losses is taken in a fixed order, so the result is deterministic.
+// partials), and the lanes are combined by xor-shuffle trees, after which
+// every lane holds the same value. The block sum of its 8 losses is taken in
+// a fixed order, so the result is deterministic.
 __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ part_m,
                                                     const float* __restrict__ part_s, int S, int rows,
                                                     const float* __restrict__ ent,
@@ -173,14 +298,19 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
   if (row < rows) {
     const float* pm = part_m + (size_t)row * S;
     const float* ps = part_s + (size_t)row * S;
-    float m = -INFINITY, s = 0.f;
-    for (int j = lane; j < S; j += 32) lse_merge(m, s, pm[j], ps[j]);
+    // Two passes with independent loads (many in flight): the row maximum
+    // M over the tile maxima, then sum_j s_j exp(m_j - M). Both in a fixed
+    // order (per lane, then an xor tree), so the result is deterministic.
+    float m = -INFINITY;
+#pragma unroll 8
+    for (int j = lane; j < S; j += 32) m = fmaxf(m, __ldg(pm + j));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      lse_merge(m, s, m2, s2);
-    }
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float s = 0.f;
+#pragma unroll 8
+    for (int j = lane; j < S; j += 32) s += __ldg(ps + j) * expf(__ldg(pm + j) - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     const float lse = m + logf(s);
     const int c = cnt[row];
     float dot = 0.f;
@@ -332,6 +462,12 @@ cudaError_t launch_transpose(const void* src, int rows, int cols, void* dst, int
 
 cudaError_t launch_prep(const int32_t* ids, const float* logp, int rows, int K, int V, int Kp, int* ids_sorted,
                         float* p_sorted, int* cnt, float* ent, int* status, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (K <= kPrepWarpK) {
+    prep_warp_kernel<<<(rows + kPrepWarpRows - 1) / kPrepWarpRows, 32 * kPrepWarpRows, 0, s>>>(
+        ids, logp, rows, K, V, Kp, ids_sorted, p_sorted, cnt, ent, status);
+    return cudaGetLastError();
+  }
   int Kpow2 = 1;
   while (Kpow2 < K) Kpow2 <<= 1;
   if (Kpow2 < kPrepThreads) Kpow2 = kPrepThreads;
