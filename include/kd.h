@@ -73,7 +73,9 @@ typedef enum kd_status {
   KD_ERR_WORKSPACE = 3,     /* ws is NULL, misaligned or smaller than required */
   KD_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed */
   KD_ERR_DEVICE_TIMEOUT = 5,/* a device-side wait exceeded its time limit */
-  KD_ERR_BAD_ID = 6         /* a cached id outside [0, V) (that entry was ignored) */
+  KD_ERR_BAD_ID = 6,        /* a cached id outside [0, V) (that entry was ignored) */
+  KD_ERR_IO = 7,            /* a cache file could not be opened, read or written */
+  KD_ERR_FORMAT = 8         /* not a cache file, an unfinished one, or a truncated one */
 } kd_status;
 
 typedef enum kd_dtype { KD_BF16 = 0, KD_F32 = 1 } kd_dtype;
@@ -200,6 +202,37 @@ KD_API int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, 
                        float grad_scale, const float* grad_scale_dev,
                        float* loss, float* lse, float* loss_rows, float* dH, float* dW,
                        int32_t accumulate_dW, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------- cache files on disk
+ *
+ * The offline cache is computed once and reused by every training run
+ * ([KD-TH] section "การทำ Distillation แบบ Offline"). These calls store it in
+ * a file and read any range of positions back. All pointers are HOST memory;
+ * none of these calls touches the GPU. Format (little-endian): a 64-byte
+ * header (magic "KDTOPK01", uint32 version 1, uint32 header size 64, int64 T,
+ * int64 V, int32 K, uint32 flags 0, 24 zero bytes), then T fixed-size
+ * records of 8*K bytes: the position's K int32 ids, then its K float32 logp.
+ * A record is what kd_topk_cache writes for one row.
+ *
+ * Writing: kd_cache_create truncates or creates `path` and returns a writer.
+ * kd_cache_append adds `rows` records from ids/logp ([rows, K] each,
+ * row-major). It returns KD_ERR_BAD_ID and writes nothing if an id lies
+ * outside [0, V). kd_cache_close syncs the data and only then records T in
+ * the header. A file whose writer never closed it keeps T = -1, and
+ * kd_cache_open rejects it with KD_ERR_FORMAT.
+ * Reading: kd_cache_open validates the header and the file size
+ * (KD_ERR_FORMAT if they disagree) and reports T, V and K (each optional).
+ * kd_cache_read copies records [row0, row0 + rows) into ids/logp. It may run
+ * concurrently from several threads on one reader. rows = 0 is a no-op for
+ * append and read (ids/logp may then be NULL). kd_cache_close releases
+ * a handle of either kind.
+ */
+typedef struct kd_cache_file kd_cache_file;
+KD_API int kd_cache_create(const char* path, int64_t V, int32_t K, kd_cache_file** out);
+KD_API int kd_cache_append(kd_cache_file* f, const int32_t* ids, const float* logp, int64_t rows);
+KD_API int kd_cache_open(const char* path, kd_cache_file** out, int64_t* T, int64_t* V, int32_t* K);
+KD_API int kd_cache_read(kd_cache_file* f, int64_t row0, int64_t rows, int32_t* ids, float* logp);
+KD_API int kd_cache_close(kd_cache_file* f);
 
 /* Synchronises `stream`, returns the status word kept in `ws` (KD_OK when no
  * device-side error was recorded) and clears it. Returns KD_ERR_CUDA if the

@@ -51,7 +51,8 @@ def test_built_for_sm103a():
 
 def test_status_strings(lib):
     for code, name in [(0, "KD_OK"), (1, "KD_ERR_INVALID_ARG"), (2, "KD_ERR_UNSUPPORTED"), (3, "KD_ERR_WORKSPACE"),
-                       (4, "KD_ERR_CUDA"), (5, "KD_ERR_DEVICE_TIMEOUT"), (6, "KD_ERR_BAD_ID")]:
+                       (4, "KD_ERR_CUDA"), (5, "KD_ERR_DEVICE_TIMEOUT"), (6, "KD_ERR_BAD_ID"),
+                       (7, "KD_ERR_IO"), (8, "KD_ERR_FORMAT")]:
         assert lib.kd_status_string(code).decode() == name
     assert lib.kd_status_string(99).decode() == "KD_ERR_UNKNOWN"
     assert lib.kd_version() >= 100

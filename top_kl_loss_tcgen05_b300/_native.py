@@ -48,6 +48,11 @@ SIGNATURES = {
         [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, ctypes.c_float, _P, _P, _P, _P, _P, _P, _I32, _P, _SZ, _P],
     ),
     "kd_read_device_status": (ctypes.c_int, [_P, _P]),
+    "kd_cache_create": (ctypes.c_int, [ctypes.c_char_p, _I64, _I32, _P]),
+    "kd_cache_append": (ctypes.c_int, [_P, _P, _P, _I64]),
+    "kd_cache_open": (ctypes.c_int, [ctypes.c_char_p, _P, _P, _P, _P]),
+    "kd_cache_read": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
+    "kd_cache_close": (ctypes.c_int, [_P]),
     "kd_test_gemm": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32, _P, _P]),
     "kd_test_wait_timeout": (ctypes.c_int, [_I64, _P, _P]),
     "kd_profile_begin": (ctypes.c_int, []),

@@ -2,7 +2,8 @@
 
     python -m top_kl_loss_tcgen05_b300.build [--force]
 
-Compiles the sources in csrc/ for sm_103a with nvcc into lib/libkd.so.
+Compiles the sources in csrc/ (CUDA for sm_103a, plus host C++) with nvcc
+into lib/libkd.so.
 A rebuild happens when a source or header is newer than the library.
 """
 
@@ -20,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libkd.so")
 
-SOURCES = ["kd_api.cu", "kd_gemm.cu", "kd_topk.cu", "kd_loss_aux.cu", "kd_noalloc.cu"]
+SOURCES = ["kd_api.cu", "kd_gemm.cu", "kd_topk.cu", "kd_loss_aux.cu", "kd_noalloc.cu", "kd_cache_io.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-Xcompiler", "-fvisibility=hidden"]
 

@@ -285,6 +285,8 @@ const char* kd_status_string(int status) {
     case KD_ERR_CUDA: return "KD_ERR_CUDA";
     case KD_ERR_DEVICE_TIMEOUT: return "KD_ERR_DEVICE_TIMEOUT";
     case KD_ERR_BAD_ID: return "KD_ERR_BAD_ID";
+    case KD_ERR_IO: return "KD_ERR_IO";
+    case KD_ERR_FORMAT: return "KD_ERR_FORMAT";
     default: return "KD_ERR_UNKNOWN";
   }
 }
