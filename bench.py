@@ -251,6 +251,49 @@ def bench_topk(dev, peaks, iters=5, rows=None):
     }
 
 
+def bench_teacher(dev, peaks, iters=5):
+    """Teacher-side cache (kd_teacher_topk_cache) on a Llama-3.1-8B-shaped LM
+    head: the projection GEMM with its LSE epilogue, and the tile-pruned
+    top-K selection. Timed alone, so the GEMM roofline uses the burst peak."""
+    c = synth.CONFIGS["teacher"]
+    T, d, V, K, chunk = c["T"], c["d"], c["V"], c["K"], c["chunk"]
+    H, W = synth.teacher_head(T, d, V, c["seed"], device=dev)
+    ws = kd.workspace(_native.lib().kd_teacher_topk_workspace_size(d, V, K, chunk), dev)
+    for _ in range(2):
+        kd.teacher_topk_cache(H, W, K, chunk=chunk, ws=ws)
+    torch.cuda.synchronize(dev)
+    _native.profile_begin()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(iters):
+        kd.teacher_topk_cache(H, W, K, chunk=chunk, ws=ws)
+    e.record()
+    torch.cuda.synchronize(dev)
+    prof = _native.profile_end()
+    ms = s.elapsed_time(e) / iters
+    gn, gms = prof.get("teacher_logits_gemm", (1, float("nan")))
+    sn, sms = prof.get("teacher_tile_topk", (1, float("nan")))
+    flops_launch = 2.0 * T * d * V * iters / gn
+    achieved = flops_launch / (gms / gn * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    exact_rows = int(ws[4:8].view(torch.int32).item())
+    del H, W, ws
+    return {
+        "workload": "teacher: H [%d, %d] x W [%d, %d] bf16 (Llama-3.1-8B-shaped LM head), K=%d, chunk=%d"
+                    % (T, d, V, d, K, chunk),
+        "ms": ms, "rows_per_s": T / (ms * 1e-3), "tflops": 2.0 * T * d * V / (ms * 1e-3) / 1e12,
+        "gemm_ms": gms / iters, "select_ms": sms / iters, "rows_on_radix_path": exact_rows // (iters + 2),
+        "workspace_gib": ws_bytes_gib(d, V, K, chunk),
+        "roofline": {"bound": "tensor", "kernel": "teacher_logits_gemm", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_kind": "bf16_tflops burst (measured)", "algorithmic_flops_per_launch": flops_launch},
+    }
+
+
+def ws_bytes_gib(d, V, K, chunk):
+    return _native.lib().kd_teacher_topk_workspace_size(d, V, K, chunk) / 2**30
+
+
 # ----------------------------------------------------------------------------- main
 
 
@@ -334,6 +377,7 @@ def main():
     ap.add_argument("--no-topk", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-fwdbwd", action="store_true", help="skip timing the single-call forward + backward")
+    ap.add_argument("--no-teacher", action="store_true", help="skip timing the teacher-side cache")
     ap.add_argument("--topk-rows", type=int, default=None, help="rows of the top-K workload (default 8192)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -518,6 +562,7 @@ def main():
                        "W (LM-head parameter), dH and dW stay on the device"}
 
     topk = None if args.no_topk else bench_topk(dev, peaks, rows=args.topk_rows)
+    teacher = None if args.no_teacher else bench_teacher(dev, peaks)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
@@ -537,6 +582,7 @@ def main():
                        else "256x256 per CTA pair (tcgen05 cta_group::2)"},
             "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
             "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "topk_extraction": topk, "fused_fwdbwd": fwdbwd,
+            "teacher_topk": teacher,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

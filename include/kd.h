@@ -110,6 +110,32 @@ KD_API int kd_topk_cache(const void* logits, int32_t dtype, int64_t T, int64_t V
                   int32_t K, int32_t* ids, float* logp, void* ws, size_t ws_bytes,
                   void* stream);
 
+/* kd_teacher_topk_cache: the same cache straight from the teacher's final
+ * hidden states and LM head, without the [T, V] logits ever existing:
+ *   H  [T, d] bf16, device: teacher final hidden states.
+ *   W  [V, d] bf16, device: teacher LM-head weights (fold any logit scale or
+ *      temperature into W).
+ * The logits x = H W^T are computed in fp32 (bf16 products, fp32
+ * accumulation on the tensor cores), one chunk of positions at a time, into
+ * the workspace. The GEMM epilogue also produces, per position and
+ * 256-column vocabulary tile, the maximum and the sum of exp for the
+ * log-sum-exp. The selection then reads only the tiles whose maximum
+ * reaches the K-th largest tile maximum: every top-K element lies in such a
+ * tile. Output contract: that of kd_topk_cache applied to the fp32 logits
+ * x (ids by value descending, then id ascending; logp = x - lse in fp32).
+ * Requires d % 8 == 0, 16-byte aligned H and W, 1 <= K <= min(V, 65536).
+ * Workspace: kd_teacher_topk_workspace_size(d, V, K, chunk) bytes
+ * (4 * chunk * round_up(V, 64) for the logits of one chunk, plus 8 bytes per
+ * position and vocabulary tile; independent of T). Its first two int32
+ * words are the status word and the running count of rows that took the
+ * exact radix path (see kd_topk_cache). This is the teacher-side fusion
+ * that the offline step needs ([KD-TH] section "การทำ Distillation แบบ
+ * Offline"). */
+KD_API size_t kd_teacher_topk_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk);
+KD_API int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_t d, int64_t V, int32_t K,
+                                 int64_t chunk, int32_t* ids, float* logp, void* ws, size_t ws_bytes,
+                                 void* stream);
+
 /* kd_topk_cache_noalloc: the same extraction, for callers that cannot
  * allocate device memory and so cannot pass a workspace. Examples: a step
  * running inside a host application that owns every device allocation

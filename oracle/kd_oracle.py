@@ -104,6 +104,14 @@ def topk_cache(logits, K: int):
     return ids, logp
 
 
+def teacher_topk_cache(H, W, K: int):
+    """The offline cache straight from the teacher's final hidden states H
+    [T, d] and LM head W [V, d]: topk_cache of the logits x = H W^T, taken in
+    fp64. This is the teacher-side path of [KD-TH] section "การทำ Distillation
+    แบบ Offline" (the teacher's projection, then its top-K)."""
+    return topk_cache(_f64(H) @ _f64(W).T, K)
+
+
 def teacher_probs(logp):
     """Cached log-probs [T, K] -> (p, log p) renormalised over the K entries.
 

@@ -251,3 +251,22 @@ def test_gradient_rows_sum_to_zero():
     ids = np.stack([rng.choice(64, 6, replace=False) for _ in range(10)])
     g = O.dlogits(z, ids, rng.normal(size=(10, 6)), 0.37)
     np.testing.assert_allclose(g.sum(1), 0.0, atol=1e-14)
+
+
+def test_teacher_topk_cache_is_the_top_k_of_H_times_W_transposed():
+    """One-hot hidden states pick single columns of the logits x = H W^T:
+    row t of H = e_j gives x[t, v] = W[v, j], so the cache of row t is the
+    top-K of column j of W. A transposed product or swapped operands would
+    give a different, shape-incompatible or wrong answer."""
+    rng = np.random.default_rng(3)
+    V, d, K = 40, 6, 5
+    W = rng.integers(-3, 4, size=(V, d)).astype(np.float64)  # many ties
+    H = np.zeros((d, d))
+    H[np.arange(d), np.arange(d)[::-1]] = 1.0  # row t selects column d-1-t
+    ids, logp = O.teacher_topk_cache(H, W, K)
+    for t in range(d):
+        col = W[:, d - 1 - t]
+        want = sorted(range(V), key=lambda v: (-col[v], v))[:K]  # value desc, id asc
+        assert list(ids[t]) == want
+        lse = np.log(np.exp(col).sum())
+        np.testing.assert_allclose(logp[t], col[want] - lse, rtol=0, atol=1e-6)

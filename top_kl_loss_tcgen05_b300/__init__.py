@@ -22,6 +22,7 @@ from ._native import KDError, check, status_string  # noqa: F401
 
 __all__ = [
     "topk_cache",
+    "teacher_topk_cache",
     "fused_kl_workspace",
     "fused_kl_fwd",
     "fused_kl_bwd",
@@ -98,6 +99,32 @@ def topk_cache(logits: torch.Tensor, K: int, ws: torch.Tensor | None = None):
         "kd_topk_cache",
         L.kd_topk_cache(logits.data_ptr(), dt, T, V, logits.stride(0), K, ids.data_ptr(), logp.data_ptr(),
                         ws.data_ptr(), ws.numel(), _stream_ptr(dev)),
+    )
+    return ids, logp
+
+
+def teacher_topk_cache(H: torch.Tensor, W: torch.Tensor, K: int, chunk: int = 1024, ws: torch.Tensor | None = None):
+    """Top-K cache straight from teacher hidden states H [T, d] bf16 and LM
+    head W [V, d] bf16 (logits computed in fp32, one chunk at a time, never
+    all at once): (ids [T, K] int32, logp [T, K] float32)."""
+    _need(H, "H", torch.bfloat16)
+    dev = H.device
+    _need(W, "W", torch.bfloat16, dev)
+    if H.dim() != 2 or W.dim() != 2 or H.shape[1] != W.shape[1]:
+        raise ValueError("H [T, d] and W [V, d] required")
+    T, d = H.shape
+    V = W.shape[0]
+    if ws is None:
+        n = _native.lib().kd_teacher_topk_workspace_size(d, V, K, chunk)
+        if n == 0:
+            raise ValueError("invalid sizes")
+        ws = workspace(n, dev)
+    ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+    logp = torch.empty(T, K, dtype=torch.float32, device=dev)
+    check(
+        "kd_teacher_topk_cache",
+        _native.lib().kd_teacher_topk_cache(H.data_ptr(), W.data_ptr(), T, d, V, K, chunk, ids.data_ptr(),
+                                            logp.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(dev)),
     )
     return ids, logp
 

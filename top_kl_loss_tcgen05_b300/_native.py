@@ -35,6 +35,8 @@ SIGNATURES = {
     "kd_topk_cache": (ctypes.c_int, [_P, _I32, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
     "kd_topk_cache_noalloc": (ctypes.c_int, [_P, _I32, _I64, _I64, _I64, _I32, _P, _P, _P]),
     "kd_fused_kl_workspace_size": (_SZ, [_I64, _I64, _I32, _I64]),
+    "kd_teacher_topk_workspace_size": (_SZ, [_I64, _I64, _I32, _I64]),
+    "kd_teacher_topk_cache": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _I64, _P, _P, _P, _SZ, _P]),
     "kd_fused_kl_fwd": (
         ctypes.c_int,
         [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, _P, _P, _P, _P, _SZ, _P],

@@ -119,15 +119,41 @@ Layout fused_layout(int64_t d, int64_t V, int K, int64_t chunk) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Teacher-cache workspace: the header, one chunk's fp32 logits
+// Z [chunk, round_up(V, 64)] and its per-(position, vocab tile) partials.
+struct TeacherLayout {
+  int64_t S, ldz;
+  size_t z, part_m, part_s, total;
+};
+
+TeacherLayout teacher_layout(int64_t V, int64_t chunk) {
+  TeacherLayout L;
+  L.S = ceil_div(V, kBNLogits);
+  L.ldz = align_up((size_t)V, 64);
+  size_t o = kHeader;
+  o = align_up(o, 1024);
+  L.z = o;
+  o += (size_t)chunk * L.ldz * 4;
+  o = align_up(o, 256);
+  L.part_m = o;
+  o += (size_t)chunk * L.S * 4;
+  o = align_up(o, 256);
+  L.part_s = o;
+  o += (size_t)chunk * L.S * 4;
+  L.total = align_up(o, 256);
+  return L;
+}
+
 // ------------------------------------------------------------------ profiling
 // Kernel names reported by kd_profile_end, indexed by KernelId.
 enum KernelId {
   K_TOPK, K_PREP, K_LOGITS_FWD, K_MERGE, K_FINALIZE, K_LOGITS_DZ, K_TRANSPOSE, K_GRAD, K_TEST, K_LOGITS_FWD_STORE,
-  K_DZ_FROM_EXP, K_COUNT
+  K_DZ_FROM_EXP, K_TEACHER_GEMM, K_TILE_TOPK, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {"topk_cache", "teacher_prep", "logits_fwd_lse_gather", "lse_merge_loss",
                                            "loss_finalize", "logits_dz", "hidden_transpose", "grad_dH_dW",
-                                           "test_gemm", "logits_fwd_store_exp", "dz_from_exp"};
+                                           "test_gemm", "logits_fwd_store_exp", "dz_from_exp",
+                                           "teacher_logits_gemm", "teacher_tile_topk"};
 struct ProfRec {
   int kid;
   cudaEvent_t a, b;
@@ -568,6 +594,75 @@ int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, const f
   }
   ProfScope ps(K_FINALIZE, s);
   return cuda_status(launch_finalize(acc, 1.0 / (double)T, loss, s));
+}
+
+size_t kd_teacher_topk_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk) {
+  if (d <= 0 || V <= 0 || K <= 0 || chunk <= 0) return 0;
+  return teacher_layout(V, chunk).total;
+}
+
+int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                          int32_t* ids, float* logp, void* ws, size_t ws_bytes, void* stream) {
+  if (!H || !W || !ids || !logp || T <= 0 || d <= 0 || V <= 0 || K <= 0 || chunk <= 0 || K > V)
+    return KD_ERR_INVALID_ARG;
+  if (V >= (int64_t(1) << 31) || K > 65536 || d % 8 != 0 || d > (int64_t(1) << 24) || chunk > (int64_t(1) << 24))
+    return KD_ERR_UNSUPPORTED;
+  if (!aligned(H, 16) || !aligned(W, 16)) return KD_ERR_UNSUPPORTED;
+  if (tile_topk_smem_bytes(K) > 200 * 1024) return KD_ERR_UNSUPPORTED;
+  const TeacherLayout L = teacher_layout(V, chunk);
+  if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return KD_ERR_WORKSPACE;
+  const int sms = num_sms_current();
+  if (sms <= 0) return KD_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* words = reinterpret_cast<int*>(w);
+  float* Z = reinterpret_cast<float*>(w + L.z);
+  float* part_m = reinterpret_cast<float*>(w + L.part_m);
+  float* part_s = reinterpret_cast<float*>(w + L.part_s);
+  const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
+  const char* fe = std::getenv("KD_TOPK_FORCE_EXACT");
+  const int force = (fe && fe[0] == '1') ? 1 : 0;
+
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.cta2 = gemm_cta2();
+  const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
+  if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
+                    BR) != cudaSuccess)
+    return KD_ERR_UNSUPPORTED;
+  for (int64_t c0 = 0; c0 < T; c0 += chunk) {
+    const int rows = (int)((T - c0) < chunk ? (T - c0) : chunk);
+    if (encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + c0 * d, (uint64_t)d, (uint64_t)rows,
+                      (uint64_t)d * 2, kBK, kBM) != cudaSuccess ||
+        encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Z, (uint64_t)V, (uint64_t)rows, (uint64_t)L.ldz * 4,
+                      32, 32) != cudaSuccess)
+      return KD_ERR_UNSUPPORTED;
+    Problem& P = a.pr[0];
+    P.m_blocks = (int)ceil_div(rows, TR);
+    P.n_blocks = (int)L.S;
+    P.k_blocks = (int)ceil_div(d, kBK);
+    P.a_mn = 0; P.b_mn = 0; P.M = rows; P.N = (int)V;
+    P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
+    a.nprob = 1;
+    a.total_tiles = P.m_blocks * P.n_blocks;
+    a.rows = rows; a.row_stride = (int)chunk; a.S = (int)L.S; a.V = (int)V;
+    a.part_m = part_m; a.part_s = part_s;
+    a.status = words;
+    a.tile_counter = reinterpret_cast<int*>(w + kCounterOffset);
+    cudaError_t e;
+    {
+      ProfScope ps(K_TEACHER_GEMM, s);
+      e = launch_logits_teacher(a, sms, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    {
+      ProfScope ps(K_TILE_TOPK, s);
+      e = launch_tile_topk(Z, L.ldz, rows, (int)V, (int)L.S, part_m, part_s, K, ids + c0 * K, logp + c0 * K, words,
+                           force, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return KD_OK;
 }
 
 int kd_read_device_status(void* ws, void* stream) {

@@ -30,7 +30,11 @@
 //     EPI_FWDST the EPI_FWD results, with the tile's maximum m as the
 //               reference, plus e = exp(z - m) -> bf16 -> TMA store, from
 //               which the single-call forward + backward forms dz without
-//               recomputing the logits.
+//               recomputing the logits;
+//     EPI_TEACHER the teacher's logits: per (row, tile) max and sum of exp
+//               (for its log-sum-exp), and the fp32 tile -> TMA store, from
+//               which the teacher top-K selection reads only the tiles that
+//               can hold a top-K element.
 // Two tile shapes:
 //   C2 = false  one CTA per 128 x 256 tile (tcgen05 cta_group::1, M = 128).
 //   C2 = true   a cluster of two CTAs per 256 x 256 tile (cta_group::2,
@@ -51,7 +55,7 @@
 namespace kd {
 namespace {
 
-constexpr int EPI_FWD = 0, EPI_DZ = 1, EPI_GRAD = 2, EPI_FWDST = 3;
+constexpr int EPI_FWD = 0, EPI_DZ = 1, EPI_GRAD = 2, EPI_FWDST = 3, EPI_TEACHER = 4;
 constexpr int kThreads = 192;  // 6 warps
 constexpr int BN = kBNLogits;  // N tile (all kernels)
 static_assert(kBNLogits == kBNGrad, "one N tile for all GEMMs");
@@ -423,7 +427,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(acc * BN);
 
-      if (EPI == EPI_FWDST) {
+      if (EPI == EPI_TEACHER) {
+        // Online (max, sum exp) over the tile's valid columns, 32 at a time,
+        // and each 32 x 32 fp32 block stored as it is read.
+        float m = -INFINITY, s = 0.f;
+        const bool box_live = m0 + 32 * wq < g.rows;
+        for (int c0 = 0; c0 < nvalid; c0 += 32) {
+          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
+          if (nstore >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+          uint32_t v[32];
+          tmem_ld32(taddr + c0, v);
+          tmem_wait_ld();
+          const int lim = nvalid - c0;
+          float cm = -INFINITY;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) if (jj < lim) cm = fmaxf(cm, u2f(v[jj]));
+          const float mn = fmaxf(m, cm);
+          const float nb2 = -mn * kLog2e;
+          float acc_s = 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) if (jj < lim) acc_s += ex2(fmaf(u2f(v[jj]), kLog2e, nb2));
+          s = s * ex2((m - mn) * kLog2e) + acc_s;
+          m = mn;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, n0 + c0, m0 + 32 * wq);
+          if (lane == 0) bulk_commit();
+          ++nstore;
+          buf ^= 1;
+        }
+        if (row < g.rows) {
+          g.part_m[(size_t)row * g.S + tl.nb] = m;
+          g.part_s[(size_t)row * g.S + tl.nb] = s;
+        }
+      } else if (EPI == EPI_FWDST) {
         // Pass 1: the row's maximum over the tile's valid columns.
         float m = -INFINITY;
         for (int c0 = 0; c0 < nvalid; c0 += 32) {
@@ -757,6 +800,10 @@ cudaError_t launch_logits_dz(const GemmArgs& a, int num_sms, cudaStream_t s) {
 cudaError_t launch_logits_fwd_store(const GemmArgs& a, int num_sms, cudaStream_t s) {
   if (a.cta2) return launch<6, EPI_FWDST, true>(a, num_sms, s);
   return launch<4, EPI_FWDST, false>(a, num_sms, s);
+}
+cudaError_t launch_logits_teacher(const GemmArgs& a, int num_sms, cudaStream_t s) {
+  if (a.cta2) return launch<6, EPI_TEACHER, true>(a, num_sms, s);
+  return launch<4, EPI_TEACHER, false>(a, num_sms, s);
 }
 cudaError_t launch_grad(const GemmArgs& a, int num_sms, cudaStream_t s) {
   if (a.cta2) return launch<6, EPI_GRAD, true>(a, num_sms, s);

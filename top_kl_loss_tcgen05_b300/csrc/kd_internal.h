@@ -67,6 +67,7 @@ cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* 
 cudaError_t launch_logits_fwd(const GemmArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_logits_dz(const GemmArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_logits_fwd_store(const GemmArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_logits_teacher(const GemmArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_grad(const GemmArgs& a, int num_sms, cudaStream_t s);
 
 // Small kernels (kd_loss_aux.cu).
@@ -87,5 +88,9 @@ cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 size_t topk_smem_bytes(int K);
 cudaError_t launch_topk(const void* logits, int dtype, int64_t T, int64_t V, int64_t ld, int K, int32_t* ids,
                         float* logp, int* ws_words, int force_exact, int num_sms, cudaStream_t stream);
+size_t tile_topk_smem_bytes(int K);
+cudaError_t launch_tile_topk(const float* Z, int64_t ldz, int rows, int V, int S, const float* part_m,
+                             const float* part_s, int K, int32_t* ids, float* logp, int* ws_words, int force_exact,
+                             cudaStream_t stream);
 
 }  // namespace kd

@@ -24,6 +24,13 @@
 //           the cache row.
 // If the buffer overflows (massive ties) or K > 1024, the row is redone by an
 // exact radix selection over the row in global memory.
+//
+// tile_topk_kernel makes the same selection from the fp32 logits that the
+// teacher GEMM wrote, using the per-(row, 256-column tile) maxima and sums
+// of exp that the GEMM epilogue produced: the log-sum-exp is merged from
+// them, tau is the K-th largest tile maximum (again K actual elements, so a
+// lower bound of the K-th value), and only tiles whose maximum reaches tau
+// are read: about K of the row's ceil(V/256) tiles.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -474,6 +481,147 @@ __global__ void __launch_bounds__(kThreads, 3) topk_kernel(const Tin* __restrict
   }
 }
 
+constexpr int kTileW = kBNLogits;     // columns per tile of the teacher GEMM
+constexpr int kTileListCap = 1024;    // tiles at or above tau read by the fast path
+
+__device__ __forceinline__ float block_max_f(float v, float* red) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < kWarps; ++i) r = fmaxf(r, red[i]);
+  __syncthreads();
+  return r;
+}
+// Sum in a fixed order (lanes by xor tree, then warps in index order).
+__device__ __forceinline__ float block_sum_f(float v, float* red) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < kWarps; ++i) r += red[i];
+  __syncthreads();
+  return r;
+}
+__device__ __forceinline__ int block_sum_i(int v, int* red) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  int r = 0;
+  for (int i = 0; i < kWarps; ++i) r += red[i];
+  __syncthreads();
+  return r;
+}
+
+// One block per row of the chunk.
+__global__ void __launch_bounds__(kThreads) tile_topk_kernel(const float* __restrict__ Z, int64_t ldz, int V, int S,
+                                                            const float* __restrict__ part_m,
+                                                            const float* __restrict__ part_s, int K,
+                                                            int force_exact, int32_t* __restrict__ ids,
+                                                            float* __restrict__ logp, int* __restrict__ ws_words) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw);  // sel_entries(K) entries
+  __shared__ uint32_t hist[256];
+  __shared__ int sm_scan[kWarps + 1];
+  __shared__ int sm_misc[4];
+  __shared__ float sm_red[kWarps];
+  __shared__ int sm_ired[kWarps];
+  __shared__ int tiles[kTileListCap];
+  __shared__ int sm_nt, sm_n;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x;
+  const float* pm = part_m + (size_t)row * S;
+  const float* ps = part_s + (size_t)row * S;
+  const float* zr = Z + (size_t)row * ldz;
+
+  // log-sum-exp of the row from the tile partials
+  float M = -INFINITY;
+  for (int j = tid; j < S; j += kThreads) M = fmaxf(M, __ldg(pm + j));
+  M = block_max_f(M, sm_red);
+  float sum = 0.f;
+  for (int j = tid; j < S; j += kThreads) sum += __ldg(ps + j) * ex2((__ldg(pm + j) - M) * kLog2e);
+  sum = block_sum_f(sum, sm_red);
+  const float lse = M + logf(sum);
+
+  bool exact = force_exact || K > kFastMaxK;
+  if (!exact) {
+    // tau: the K-th largest tile maximum (key 0 = take every tile)
+    uint32_t kth = 0;
+    if (S > K) {
+      for (int b = 31; b >= 0; --b) {
+        const uint32_t c = kth | (1u << b);
+        int cnt = 0;
+        for (int j = tid; j < S; j += kThreads) cnt += okey(__ldg(pm + j)) >= c;
+        if (block_sum_i(cnt, sm_ired) >= K) kth = c;
+      }
+    }
+    if (tid == 0) { sm_nt = 0; sm_n = 0; }
+    __syncthreads();
+    for (int j = tid; j < S; j += kThreads) {
+      if (okey(__ldg(pm + j)) >= kth) {
+        const int p = atomicAdd(&sm_nt, 1);
+        if (p < kTileListCap) tiles[p] = j;
+      }
+    }
+    __syncthreads();
+    const int nt = sm_nt;
+    if (nt > kTileListCap) {
+      exact = true;
+    } else {
+      // a warp per listed tile: 32 lanes x 8 consecutive columns
+      for (int i = warp; i < nt; i += kWarps) {
+        const int c0 = tiles[i] * kTileW + lane * 8;
+        float x[8];
+        if (c0 + 8 <= V) {
+          const float4 a = __ldg(reinterpret_cast<const float4*>(zr + c0));
+          const float4 b = __ldg(reinterpret_cast<const float4*>(zr + c0 + 4));
+          x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) x[j] = c0 + j < V ? __ldg(zr + c0 + j) : -INFINITY;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (c0 + j < V && okey(x[j]) >= kth) {
+            const int p = atomicAdd(&sm_n, 1);
+            if (p < kCandCap) cand[p] = rkey(x[j], (uint32_t)(c0 + j));
+          }
+        }
+      }
+      __syncthreads();
+      const int n = sm_n;
+      if (n > kCandCap || n < K) {
+        exact = true;
+      } else {
+        int n2 = 1;
+        while (n2 < n) n2 <<= 1;
+        for (int i = n + tid; i < n2; i += kThreads) cand[i] = 0;
+        __syncthreads();
+        bitonic_desc(cand, n2);
+      }
+    }
+  }
+  if (exact) {
+    if (tid == 0 && !force_exact) atomicAdd(&ws_words[1], 1);
+    __syncthreads();
+    int kp2 = 1;
+    while (kp2 < K) kp2 <<= 1;
+    exact_select<float>(zr, V, K, cand, kp2, hist, sm_scan, sm_misc);
+  }
+  __syncthreads();
+  for (int k = tid; k < K; k += kThreads) {
+    const uint64_t c = cand[k];
+    ids[(int64_t)row * K + k] = (int32_t)(0xFFFFFFFFu - (uint32_t)c);
+    logp[(int64_t)row * K + k] = okey_to_float((uint32_t)(c >> 32)) - lse;
+  }
+}
+
 }  // namespace
 
 // Entries of the candidate / exact-path buffer: the fast path's candidate
@@ -485,6 +633,19 @@ static int sel_entries(int K) {
 }
 
 size_t topk_smem_bytes(int K) { return (size_t)sel_entries(K) * sizeof(uint64_t); }
+size_t tile_topk_smem_bytes(int K) { return topk_smem_bytes(K); }
+
+cudaError_t launch_tile_topk(const float* Z, int64_t ldz, int rows, int V, int S, const float* part_m,
+                             const float* part_s, int K, int32_t* ids, float* logp, int* ws_words, int force_exact,
+                             cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const size_t smem = tile_topk_smem_bytes(K);
+  cudaError_t e = cudaFuncSetAttribute(tile_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  tile_topk_kernel<<<rows, kThreads, smem, stream>>>(Z, ldz, V, S, part_m, part_s, K, force_exact, ids, logp,
+                                                    ws_words);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_topk(const void* logits, int dtype, int64_t T, int64_t V, int64_t ld, int K,
                         int32_t* ids, float* logp, int* ws_words, int force_exact, int num_sms,

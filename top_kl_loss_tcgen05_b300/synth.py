@@ -13,6 +13,9 @@ Workloads (sizes from the pages' settings):
 * Top-K extraction logits: N(0, 2) plus a Zipf-like per-row bias
   b_t[v] = -log(1 + ((v + o_t) mod V)), where o_t is uniform per row. Stored
   as bf16.
+* Teacher head (teacher-side cache): H ~ N(0, 1) [T, d] and W ~ N(0, 3.375/d)
+  [V, d], both bf16, so each logit has variance 3.375 = 1.5^2 * (1 + 0.5), the
+  variance of the perturbed-W teacher logits above.
 * Synthetic cache: K distinct ids per row, (a_t + k * b_t) mod V with
   gcd(b_t, V) = 1, and log-probs that are a descending N(0, 2) sample shifted
   down by log V. The loss renormalises them over K.
@@ -31,6 +34,7 @@ __all__ = [
     "teacher_logits_from",
     "teacher_logits",
     "topk_logits",
+    "teacher_head",
     "synthetic_cache",
 ]
 
@@ -44,6 +48,8 @@ CONFIGS = {
     "gptoss20b": dict(T=32768, d=2880, V=201088, K=100, chunk=2048, seed=1002),
     "long": dict(T=262144, d=2880, V=201088, K=100, chunk=4096, seed=1003),
     "topk": dict(T=8192, V=201088, K=100, seed=1004),
+    # teacher-side cache straight from a Llama-3.1-8B-shaped LM head
+    "teacher": dict(T=8192, d=4096, V=128256, K=100, chunk=1024, seed=1005),
 }
 
 
@@ -58,6 +64,17 @@ def student(T: int, d: int, V: int, seed: int, device="cpu"):
     g = _gen(seed, device)
     H = torch.randn(T, d, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
     W = (torch.randn(V, d, generator=g, device=device, dtype=torch.float32) * (1.0 / math.sqrt(d))).to(
+        torch.bfloat16
+    )
+    return H, W
+
+
+def teacher_head(T: int, d: int, V: int, seed: int, device="cpu"):
+    """Teacher final hidden states H [T, d] ~ N(0, 1) and LM head W [V, d] ~
+    N(0, 3.375/d), drawn in fp32 then rounded to bf16."""
+    g = _gen(seed, device)
+    H = torch.randn(T, d, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    W = (torch.randn(V, d, generator=g, device=device, dtype=torch.float32) * math.sqrt(3.375 / d)).to(
         torch.bfloat16
     )
     return H, W
