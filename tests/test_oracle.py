@@ -270,3 +270,100 @@ def test_teacher_topk_cache_is_the_top_k_of_H_times_W_transposed():
         assert list(ids[t]) == want
         lse = np.log(np.exp(col).sum())
         np.testing.assert_allclose(logp[t], col[want] - lse, rtol=0, atol=1e-6)
+
+
+# ------------------------------------------------------- temperature and mask
+
+
+def test_temperature_limit_is_log_V_over_K():
+    """As tau grows, the tempered teacher tends to uniform over its K ids and
+    the tempered student to uniform over V, so L -> log(V / K). A missing
+    division of z or of the teacher log-probs by tau would not converge."""
+    rng = np.random.default_rng(20)
+    T, V, K = 3, 50, 7
+    z = rng.normal(0, 2, size=(T, V))
+    ids = np.stack([rng.choice(V, K, replace=False) for _ in range(T)])
+    logp = rng.normal(0, 2, size=(T, K))
+    L, _ = O.kl_rows_from_logits(z, ids, logp, temperature=1e6)
+    np.testing.assert_allclose(L, math.log(V / K), rtol=0, atol=1e-5)
+
+
+def test_temperature_keeps_gibbs_and_kl_zero():
+    """KL >= 0 at every tau, and = 0 when the tempered student equals the
+    tempered teacher: z = logp on the K ids (and -inf elsewhere)."""
+    rng = np.random.default_rng(21)
+    T, V, K = 4, 30, 6
+    ids = np.stack([rng.choice(V, K, replace=False) for _ in range(T)])
+    logp = rng.normal(0, 1, size=(T, K))
+    for tau in (0.3, 1.0, 2.5):
+        z = rng.normal(0, 2, size=(T, V))
+        L, _ = O.kl_rows_from_logits(z, ids, logp, temperature=tau)
+        assert np.all(L >= -1e-12)
+        z0 = np.full((T, V), -1e300)
+        z0[np.arange(T)[:, None], ids] = logp + 3.0  # any shift: softmax is shift-invariant
+        L0, _ = O.kl_rows_from_logits(z0, ids, logp, temperature=tau)
+        np.testing.assert_allclose(L0, 0.0, atol=1e-12)
+
+
+@pytest.mark.parametrize("tau", [0.7, 2.5])
+def test_tempered_gradient_matches_finite_differences(tau):
+    """dL/dz = (1/tau) (q_tau - p_tau): a dropped 1/tau fails."""
+    rng = np.random.default_rng(22)
+    T, V, K = 3, 11, 4
+    z = rng.normal(0, 1.5, size=(T, V))
+    ids = np.stack([rng.choice(V, K, replace=False) for _ in range(T)])
+    logp = rng.normal(0, 1, size=(T, K))
+    fd = _fd(lambda: O.kl_rows_from_logits(z, ids, logp, temperature=tau)[0].sum(), z)
+    np.testing.assert_allclose(O.dlogits(z, ids, logp, 1.0, temperature=tau), fd, rtol=1e-6, atol=1e-9)
+
+
+def test_mask_excludes_positions_and_normalises_over_the_rest():
+    """The masked loss is the loss of the included positions alone (computed
+    without a mask on that subset); excluded rows of dH are zero; dW is the
+    subset's dW; finite differences on H and W pin the 1/N normalisation."""
+    rng = np.random.default_rng(23)
+    T, d, V, K = 6, 5, 9, 3
+    H = rng.normal(0, 1, size=(T, d))
+    W = rng.normal(0, 0.5, size=(V, d))
+    ids = np.stack([rng.choice(V, K, replace=False) for _ in range(T)])
+    logp = rng.normal(0, 1, size=(T, K))
+    mask = np.array([1, 0, 1, 1, 0, 1], dtype=np.uint8)
+    keep = mask.astype(bool)
+    n = int(keep.sum())
+    loss_n, lse, L = O.fused_kl_forward(H, W, ids, logp, mask=mask, mean_over_mask=True)
+    loss_sub, lse_sub, L_sub = O.fused_kl_forward(H[keep], W, ids[keep], logp[keep])
+    assert abs(loss_n - loss_sub) <= 1e-14 * abs(loss_sub)
+    np.testing.assert_array_equal(L[~keep], 0.0)
+    np.testing.assert_allclose(L[keep], L_sub, rtol=1e-14)
+    loss_T, _, _ = O.fused_kl_forward(H, W, ids, logp, mask=mask, mean_over_mask=False)
+    assert abs(loss_T - loss_sub * n / T) <= 1e-14 * abs(loss_T)
+    dH, dW = O.fused_kl_backward(H, W, ids, logp, 1.0 / n, mask=mask)
+    dH_sub, dW_sub = O.fused_kl_backward(H[keep], W, ids[keep], logp[keep], 1.0 / n)
+    np.testing.assert_array_equal(dH[~keep], 0.0)
+    np.testing.assert_allclose(dH[keep], dH_sub, rtol=1e-13)
+    np.testing.assert_allclose(dW, dW_sub, rtol=1e-13, atol=1e-16)
+
+    def loss():
+        return O.fused_kl_forward(H, W, ids, logp, mask=mask, mean_over_mask=True)[0]
+
+    np.testing.assert_allclose(dH, _fd(loss, H), rtol=1e-6, atol=1e-10)
+    np.testing.assert_allclose(dW, _fd(loss, W), rtol=1e-6, atol=1e-10)
+    lossz, _, Lz = O.fused_kl_forward(H, W, ids, logp, mask=np.zeros(T), mean_over_mask=True)
+    assert lossz == 0.0 and np.all(Lz == 0.0)
+
+
+def test_tempered_masked_dH_dW_match_finite_differences():
+    rng = np.random.default_rng(24)
+    T, d, V, K, tau = 4, 4, 8, 3, 1.7
+    H = rng.normal(0, 1, size=(T, d))
+    W = rng.normal(0, 0.5, size=(V, d))
+    ids = np.stack([rng.choice(V, K, replace=False) for _ in range(T)])
+    logp = rng.normal(0, 1, size=(T, K))
+    mask = np.array([1, 1, 0, 1])
+
+    def loss():
+        return O.fused_kl_forward(H, W, ids, logp, temperature=tau, mask=mask, mean_over_mask=False)[0]
+
+    dH, dW = O.fused_kl_backward(H, W, ids, logp, 1.0 / T, temperature=tau, mask=mask)
+    np.testing.assert_allclose(dH, _fd(loss, H), rtol=1e-6, atol=1e-10)
+    np.testing.assert_allclose(dW, _fd(loss, W), rtol=1e-6, atol=1e-10)
