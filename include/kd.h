@@ -229,6 +229,54 @@ KD_API int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, 
                        float* loss, float* lse, float* loss_rows, float* dH, float* dW,
                        int32_t accumulate_dW, void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------- loss variants (_ex)
+ *
+ * kd_fused_kl_fwd_ex / kd_fused_kl_bwd_ex / kd_fused_kl_fwdbwd_ex take the
+ * arguments of the plain calls plus `opt`, just before `ws`. opt == NULL
+ * gives exactly the plain calls. The pages leave these variants open; they
+ * follow the usual distillation conventions.
+ *   temperature     tau > 0 (1 = none). The student distribution is
+ *                   softmax(z / tau) and the teacher's is its cached
+ *                   log-probs divided by tau, renormalised over K. lse is
+ *                   that of z / tau, and dL/dz gains a factor 1/tau. No
+ *                   tau^2 factor is applied; to use Hinton's scaling,
+ *                   multiply the loss and grad_scale by tau^2.
+ *   mask            [T] uint8, device, or NULL. A position with mask[t] == 0
+ *                   adds nothing to the loss (its loss_rows entry is 0),
+ *                   gets a zero dH row and contributes nothing to dW.
+ *   mean_over_mask  0: loss = sum_t L_t / T, and grad_scale carries the
+ *                   reduction as in the plain calls (1/T for the mean).
+ *                   1: loss = sum_t L_t / N with N = the included positions
+ *                   (loss 0 if N = 0); the backward then applies 1/N itself,
+ *                   so grad_scale is d objective / d loss (1 for the loss
+ *                   alone). N is counted on the device; nothing synchronises.
+ *   dH_bf16         1: dH is written as bf16 [T, d] (dH points to bf16).
+ * An invalid option (tau <= 0 or not finite, flags outside {0, 1}) returns
+ * KD_ERR_INVALID_ARG.
+ */
+typedef struct kd_kl_options {
+  float temperature;
+  const uint8_t* mask;
+  int32_t mean_over_mask;
+  int32_t dH_bf16;
+} kd_kl_options;
+
+KD_API int kd_fused_kl_fwd_ex(const void* H, const void* W, const int32_t* ids, const float* logp,
+                              int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                              float* loss, float* lse, float* loss_rows, const kd_kl_options* opt,
+                              void* ws, size_t ws_bytes, void* stream);
+KD_API int kd_fused_kl_bwd_ex(const void* H, const void* W, const int32_t* ids, const float* logp,
+                              const float* lse, int64_t T, int64_t d, int64_t V, int32_t K,
+                              int64_t chunk, float grad_scale, const float* grad_scale_dev,
+                              void* dH, float* dW, int32_t accumulate_dW, const kd_kl_options* opt,
+                              void* ws, size_t ws_bytes, void* stream);
+KD_API int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, const float* logp,
+                                 int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                                 float grad_scale, const float* grad_scale_dev,
+                                 float* loss, float* lse, float* loss_rows, void* dH, float* dW,
+                                 int32_t accumulate_dW, const kd_kl_options* opt,
+                                 void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------- cache files on disk
  *
  * The offline cache is computed once and reused by every training run

@@ -15,6 +15,8 @@ top-K cache) and "กลไก Fused Chunked KL Loss" (the fused chunked loss).
 
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
 from . import _native
@@ -152,102 +154,146 @@ def _check_fused(H, W, ids, logp):
     return H.shape[0], H.shape[1], W.shape[0], ids.shape[1]
 
 
-def fused_kl_fwd(H, W, ids, logp, chunk: int, ws=None, want_rows: bool = False):
-    """Forward: (loss [] f32, lse [T] f32, loss_rows [T] f32 or None)."""
+def _options(T, dev, temperature, mask, mean_over_mask, dH_bf16):
+    """kd_kl_options for the _ex calls, or None when every option is at its
+    default (the plain behaviour). Returns (struct or None, mask tensor)."""
+    if temperature == 1.0 and mask is None and not mean_over_mask and not dH_bf16:
+        return None, None
+    m = None
+    if mask is not None:
+        m = mask
+        if m.dtype == torch.bool:
+            m = m.view(torch.uint8)
+        _need(m, "mask", torch.uint8, dev)
+        if m.dim() != 1 or m.shape[0] != T:
+            raise ValueError("mask must be [T]")
+    o = _native.KLOptions(float(temperature), m.data_ptr() if m is not None else None, 1 if mean_over_mask else 0,
+                          1 if dH_bf16 else 0)
+    return o, m
+
+
+def _optp(o):
+    return ctypes.byref(o) if o is not None else None
+
+
+def fused_kl_fwd(H, W, ids, logp, chunk: int, ws=None, want_rows: bool = False, temperature: float = 1.0,
+                 mask=None, mean_over_mask: bool = False):
+    """Forward: (loss [] f32, lse [T] f32, loss_rows [T] f32 or None).
+
+    temperature, mask and mean_over_mask are the kd_kl_options of
+    include/kd.h (student softmax(z / tau), tempered teacher; positions with
+    mask == 0 excluded; the mean over T or over the included positions)."""
     T, d, V, K = _check_fused(H, W, ids, logp)
     dev = H.device
     if ws is None:
         ws = fused_kl_workspace(d, V, K, chunk, dev)
+    o, _m = _options(T, dev, temperature, mask, mean_over_mask, False)
     loss = torch.empty((), dtype=torch.float32, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
     rows = torch.empty(T, dtype=torch.float32, device=dev) if want_rows else None
     check(
-        "kd_fused_kl_fwd",
-        _native.lib().kd_fused_kl_fwd(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K,
-                                      chunk, loss.data_ptr(), lse.data_ptr(), _ptr(rows), ws.data_ptr(),
-                                      ws.numel(), _stream_ptr(dev)),
+        "kd_fused_kl_fwd_ex",
+        _native.lib().kd_fused_kl_fwd_ex(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K,
+                                         chunk, loss.data_ptr(), lse.data_ptr(), _ptr(rows), _optp(o),
+                                         ws.data_ptr(), ws.numel(), _stream_ptr(dev)),
     )
     return loss, lse, rows
 
 
 def fused_kl_bwd(H, W, ids, logp, lse, chunk: int, grad_scale: float, grad_scale_dev=None, dH=None, dW=None,
-                 accumulate_dW: bool = False, ws=None):
-    """Backward: (dH [T, d] f32, dW [V, d] f32) for dz = s (q - p)."""
+                 accumulate_dW: bool = False, ws=None, temperature: float = 1.0, mask=None,
+                 mean_over_mask: bool = False, dH_bf16: bool = False):
+    """Backward: (dH [T, d] f32 (bf16 with dH_bf16), dW [V, d] f32) for
+    dz = s (q - p); s = grad_scale * grad_scale_dev * 1/tau, times 1/N when
+    mean_over_mask (then grad_scale is d objective / d loss)."""
     T, d, V, K = _check_fused(H, W, ids, logp)
     dev = H.device
     _need(lse, "lse", torch.float32, dev)
     if ws is None:
         ws = fused_kl_workspace(d, V, K, chunk, dev)
+    dh_dtype = torch.bfloat16 if dH_bf16 else torch.float32
     if dH is None:
-        dH = torch.empty(T, d, dtype=torch.float32, device=dev)
+        dH = torch.empty(T, d, dtype=dh_dtype, device=dev)
     if dW is None:
         dW = torch.empty(V, d, dtype=torch.float32, device=dev)
-    _need(dH, "dH", torch.float32, dev)
+    _need(dH, "dH", dh_dtype, dev)
     _need(dW, "dW", torch.float32, dev)
     if grad_scale_dev is not None:
         _need(grad_scale_dev, "grad_scale_dev", torch.float32, dev)
+    o, _m = _options(T, dev, temperature, mask, mean_over_mask, dH_bf16)
     check(
-        "kd_fused_kl_bwd",
-        _native.lib().kd_fused_kl_bwd(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), lse.data_ptr(),
-                                      T, d, V, K, chunk, float(grad_scale), _ptr(grad_scale_dev), dH.data_ptr(),
-                                      dW.data_ptr(), 1 if accumulate_dW else 0, ws.data_ptr(), ws.numel(),
-                                      _stream_ptr(dev)),
+        "kd_fused_kl_bwd_ex",
+        _native.lib().kd_fused_kl_bwd_ex(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(),
+                                         lse.data_ptr(), T, d, V, K, chunk, float(grad_scale), _ptr(grad_scale_dev),
+                                         dH.data_ptr(), dW.data_ptr(), 1 if accumulate_dW else 0, _optp(o),
+                                         ws.data_ptr(), ws.numel(), _stream_ptr(dev)),
     )
     return dH, dW
 
 
 def fused_kl_fwdbwd(H, W, ids, logp, chunk: int, grad_scale: float | None = None, grad_scale_dev=None, dH=None,
-                    dW=None, accumulate_dW: bool = False, ws=None, want_rows: bool = False):
+                    dW=None, accumulate_dW: bool = False, ws=None, want_rows: bool = False, temperature: float = 1.0,
+                    mask=None, mean_over_mask: bool = False, dH_bf16: bool = False):
     """Forward and backward in one call, without recomputing the logits:
-    (loss, lse, loss_rows or None, dH, dW). grad_scale defaults to 1/T (the
-    gradient of the mean loss itself)."""
+    (loss, lse, loss_rows or None, dH, dW). grad_scale defaults to the
+    gradient of the loss itself: 1/T, or 1 with mean_over_mask (the library
+    then applies 1/N)."""
     T, d, V, K = _check_fused(H, W, ids, logp)
     dev = H.device
     if ws is None:
         ws = fused_kl_workspace(d, V, K, chunk, dev)
     if grad_scale is None:
-        grad_scale = 1.0 / T
+        grad_scale = 1.0 if (mean_over_mask and mask is not None) else 1.0 / T
     loss = torch.empty((), dtype=torch.float32, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
     rows = torch.empty(T, dtype=torch.float32, device=dev) if want_rows else None
+    dh_dtype = torch.bfloat16 if dH_bf16 else torch.float32
     if dH is None:
-        dH = torch.empty(T, d, dtype=torch.float32, device=dev)
+        dH = torch.empty(T, d, dtype=dh_dtype, device=dev)
     if dW is None:
         dW = torch.empty(V, d, dtype=torch.float32, device=dev)
-    _need(dH, "dH", torch.float32, dev)
+    _need(dH, "dH", dh_dtype, dev)
     _need(dW, "dW", torch.float32, dev)
     if grad_scale_dev is not None:
         _need(grad_scale_dev, "grad_scale_dev", torch.float32, dev)
+    o, _m = _options(T, dev, temperature, mask, mean_over_mask, dH_bf16)
     check(
-        "kd_fused_kl_fwdbwd",
-        _native.lib().kd_fused_kl_fwdbwd(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K,
-                                         chunk, float(grad_scale), _ptr(grad_scale_dev), loss.data_ptr(),
-                                         lse.data_ptr(), _ptr(rows), dH.data_ptr(), dW.data_ptr(),
-                                         1 if accumulate_dW else 0, ws.data_ptr(), ws.numel(), _stream_ptr(dev)),
+        "kd_fused_kl_fwdbwd_ex",
+        _native.lib().kd_fused_kl_fwdbwd_ex(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K,
+                                            chunk, float(grad_scale), _ptr(grad_scale_dev), loss.data_ptr(),
+                                            lse.data_ptr(), _ptr(rows), dH.data_ptr(), dW.data_ptr(),
+                                            1 if accumulate_dW else 0, _optp(o), ws.data_ptr(), ws.numel(),
+                                            _stream_ptr(dev)),
     )
     return loss, lse, rows, dH, dW
 
 
 class FusedKL(torch.autograd.Function):
-    """loss = mean_t KL(p_teacher,topK || softmax(W h_t)), fused and chunked.
+    """loss = mean KL(p_teacher,topK || softmax(W h_t)), fused and chunked.
 
-    Forward saves only lse [T] (4 bytes per position). Backward recomputes
-    each chunk's logits. The upstream gradient goes to the kernels as a
-    device scalar, so backward does not synchronise.
+    FusedKL.apply(H, W, ids, logp, chunk, temperature=1.0, mask=None,
+    mean_over_mask=False). Forward saves only lse [T] (4 bytes per
+    position). Backward recomputes each chunk's logits. The upstream gradient
+    goes to the kernels as a device scalar, so backward does not synchronise.
+    dH comes out of the kernels in H's dtype when H is bf16.
     """
 
     @staticmethod
-    def forward(ctx, H, W, ids, logp, chunk: int):
+    def forward(ctx, H, W, ids, logp, chunk: int, temperature: float = 1.0, mask=None, mean_over_mask: bool = False):
         ws = fused_kl_workspace(H.shape[1], W.shape[0], ids.shape[1], chunk, H.device)
-        loss, lse, _ = fused_kl_fwd(H, W, ids, logp, chunk, ws=ws)
+        loss, lse, _ = fused_kl_fwd(H, W, ids, logp, chunk, ws=ws, temperature=temperature, mask=mask,
+                                    mean_over_mask=mean_over_mask)
         ctx.save_for_backward(H, W, ids, logp, lse)
-        ctx.chunk = chunk
-        ctx.ws = ws
+        ctx.chunk, ctx.ws = chunk, ws
+        ctx.temperature, ctx.mask, ctx.mean_over_mask = temperature, mask, mean_over_mask
         return loss
 
     @staticmethod
     def backward(ctx, g):
         H, W, ids, logp, lse = ctx.saved_tensors
         g = g.detach().to(torch.float32).contiguous()
-        dH, dW = fused_kl_bwd(H, W, ids, logp, lse, ctx.chunk, 1.0 / H.shape[0], grad_scale_dev=g, ws=ctx.ws)
-        return dH.to(H.dtype), dW.to(W.dtype), None, None, None
+        over_mask = bool(ctx.mean_over_mask) and ctx.mask is not None
+        dH, dW = fused_kl_bwd(H, W, ids, logp, lse, ctx.chunk, 1.0 if over_mask else 1.0 / H.shape[0],
+                              grad_scale_dev=g, ws=ctx.ws, temperature=ctx.temperature, mask=ctx.mask,
+                              mean_over_mask=ctx.mean_over_mask, dH_bf16=H.dtype == torch.bfloat16)
+        return dH, dW, None, None, None, None, None, None

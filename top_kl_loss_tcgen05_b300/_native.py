@@ -49,6 +49,19 @@ SIGNATURES = {
         ctypes.c_int,
         [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, ctypes.c_float, _P, _P, _P, _P, _P, _P, _I32, _P, _SZ, _P],
     ),
+    "kd_fused_kl_fwd_ex": (
+        ctypes.c_int,
+        [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, _P, _P, _P, _P, _P, _SZ, _P],
+    ),
+    "kd_fused_kl_bwd_ex": (
+        ctypes.c_int,
+        [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, ctypes.c_float, _P, _P, _P, _I32, _P, _P, _SZ, _P],
+    ),
+    "kd_fused_kl_fwdbwd_ex": (
+        ctypes.c_int,
+        [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, ctypes.c_float, _P, _P, _P, _P, _P, _P, _I32, _P, _P, _SZ,
+         _P],
+    ),
     "kd_read_device_status": (ctypes.c_int, [_P, _P]),
     "kd_cache_create": (ctypes.c_int, [ctypes.c_char_p, _I64, _I32, _P]),
     "kd_cache_append": (ctypes.c_int, [_P, _P, _P, _I64]),
@@ -60,6 +73,13 @@ SIGNATURES = {
     "kd_profile_begin": (ctypes.c_int, []),
     "kd_profile_end": (ctypes.c_int, [_P, _I32, _P]),
 }
+
+
+class KLOptions(ctypes.Structure):
+    """Mirror of kd_kl_options in include/kd.h."""
+
+    _fields_ = [("temperature", ctypes.c_float), ("mask", ctypes.c_void_p), ("mean_over_mask", ctypes.c_int32),
+                ("dH_bf16", ctypes.c_int32)]
 
 
 class ProfEntry(ctypes.Structure):

@@ -13,6 +13,7 @@
 // The only per-group buffers (in the caller's workspace) are O(G * chunk * V):
 // the bf16 dz of one group and the per-tile partials. Nothing grows with T
 // apart from the caller's own inputs and outputs.
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -38,6 +39,7 @@ constexpr size_t kHeader = 256;  // status word, counters, fp64 loss accumulator
 constexpr size_t kCounterOffset = 64;  // int: tile counter of the GEMM launches
 constexpr size_t kAccOffset = 128;
 constexpr size_t kDoneOffset = 136;    // unsigned: blocks of the current merge launch that finished
+constexpr size_t kScaleOffset = 144;   // float: the backward's per-position gradient factor
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -214,8 +216,9 @@ int check_fused_args(const void* H, const void* W, const int32_t* ids, const flo
 
 }  // namespace
 
-cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+namespace {
+cudaError_t encode_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
   std::call_once(g_encode_once, load_encode);
   if (!g_encode) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {inner, outer};
@@ -223,9 +226,19 @@ cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* 
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+}  // namespace
+
+cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return encode_map(map, dt, base, inner, outer, row_bytes, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+cudaError_t encode_map_2d_plain(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                                uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return encode_map(map, dt, base, inner, outer, row_bytes, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 namespace {
@@ -238,8 +251,8 @@ namespace {
 // `ag` carries the tensor maps of W (tmA[0]) and dW (tmC[1]) set up once
 // per call.
 int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __nv_bfloat16* dz,
-               __nv_bfloat16* hct, float* dH, int64_t g0, int grows, int64_t d, int64_t V, int reduce_add,
-               int sms, cudaStream_t s) {
+               __nv_bfloat16* hct, void* dH, int dH_bf16, int64_t g0, int grows, int64_t d, int64_t V,
+               int reduce_add, int sms, cudaStream_t s) {
   const int TR = gemm_tile_rows(ag.cta2), BR = gemm_b_box_rows(ag.cta2);
   cudaError_t e;
   {
@@ -247,10 +260,15 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
     e = launch_transpose(Hb + g0 * d, grows, (int)d, hct, (int)L.ldt, s);
   }
   if (e != cudaSuccess) return cuda_status(e);
-  if (encode_map_2d(&ag.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
+  const cudaError_t eh =
+      dH_bf16 ? encode_map_2d_plain(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                    static_cast<__nv_bfloat16*>(dH) + g0 * d, (uint64_t)d, (uint64_t)grows,
+                                    (uint64_t)d * 2, 32, 32)
+              : encode_map_2d(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, static_cast<float*>(dH) + g0 * d,
+                              (uint64_t)d, (uint64_t)grows, (uint64_t)d * 4, 32, 32);
+  if (eh != cudaSuccess ||
+      encode_map_2d(&ag.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
                     (uint64_t)L.ldz * 2, kBK, BR) != cudaSuccess ||
-      encode_map_2d(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dH + g0 * d, (uint64_t)d, (uint64_t)grows,
-                    (uint64_t)d * 4, 32, 32) != cudaSuccess ||
       encode_map_2d(&ag.tmA[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
                     (uint64_t)L.ldz * 2, 64, 64) != cudaSuccess ||
       encode_map_2d(&ag.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, hct, (uint64_t)grows, (uint64_t)d,
@@ -261,7 +279,7 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
   P0.n_blocks = (int)ceil_div(grows, kBNGrad);
   P0.k_blocks = (int)ceil_div(V, kBK);
   P0.a_mn = 1; P0.b_mn = 0; P0.M = (int)d; P0.N = grows;
-  P0.tile_begin = 0; P0.n_fastest = 0; P0.reduce_add = 0; P0.c_trans = 1;
+  P0.tile_begin = 0; P0.n_fastest = 0; P0.reduce_add = 0; P0.c_trans = 1; P0.out_bf16 = dH_bf16;
   Problem& P1 = ag.pr[1];
   P1.m_blocks = (int)ceil_div(V, TR);
   P1.n_blocks = (int)ceil_div(d, kBNGrad);
@@ -269,7 +287,7 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
   P1.a_mn = 1; P1.b_mn = 0; P1.M = (int)V; P1.N = (int)d;
   P1.tile_begin = P0.m_blocks * P0.n_blocks; P1.n_fastest = 1;
   P1.reduce_add = reduce_add;
-  P1.c_trans = 0;
+  P1.c_trans = 0; P1.out_bf16 = 0;
   ag.nprob = 2;
   ag.total_tiles = P1.tile_begin + P1.m_blocks * P1.n_blocks;
   {
@@ -293,6 +311,32 @@ int grad_setup(GemmArgs& ag, const void* W, float* dW, int64_t d, int64_t V, int
     return KD_ERR_UNSUPPORTED;
   return KD_OK;
 }
+
+// Loss options of the _ex calls, validated (NULL = the plain calls).
+struct LossOpts {
+  float inv_tau = 1.f;
+  const uint8_t* mask = nullptr;
+  int mean_over_mask = 0;
+  int dH_bf16 = 0;
+};
+
+int parse_opts(const kd_kl_options* o, LossOpts* out) {
+  LossOpts r;
+  if (o) {
+    if (!(o->temperature > 0.f) || !std::isfinite(o->temperature) || !std::isfinite(1.f / o->temperature))
+      return KD_ERR_INVALID_ARG;
+    if ((o->mean_over_mask != 0 && o->mean_over_mask != 1) || (o->dH_bf16 != 0 && o->dH_bf16 != 1))
+      return KD_ERR_INVALID_ARG;
+    r.inv_tau = 1.f / o->temperature;
+    r.mask = o->mask;
+    r.mean_over_mask = o->mean_over_mask;
+    r.dH_bf16 = o->dH_bf16;
+  }
+  *out = r;
+  return KD_OK;
+}
+
+const uint8_t* mask_at(const LossOpts& o, int64_t row0) { return o.mask ? o.mask + row0 : nullptr; }
 
 }  // namespace
 
@@ -346,12 +390,14 @@ size_t kd_fused_kl_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk
   return fused_layout(d, V, K, chunk).total;
 }
 
-int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
-                    int64_t V, int32_t K, int64_t chunk, float* loss, float* lse, float* loss_rows, void* ws,
-                    size_t ws_bytes, void* stream) {
+int kd_fused_kl_fwd_ex(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
+                       int64_t V, int32_t K, int64_t chunk, float* loss, float* lse, float* loss_rows,
+                       const kd_kl_options* opt, void* ws, size_t ws_bytes, void* stream) {
   int st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, ws, ws_bytes);
   if (st != KD_OK) return st;
   if (!loss || !lse) return KD_ERR_INVALID_ARG;
+  LossOpts o;
+  if ((st = parse_opts(opt, &o)) != KD_OK) return st;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -371,16 +417,17 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
   // The merge kernels count finished blocks in the workspace header; the
   // count returns to 0 after every launch, and starts there for this call.
-  cudaError_t e0 = cudaMemsetAsync(done, 0, sizeof(unsigned), s);
-  if (e0 != cudaSuccess) return cuda_status(e0);
+  cudaError_t e = cudaMemsetAsync(done, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return cuda_status(e);
 
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.cta2 = gemm_cta2();
+  a.zscale = o.inv_tau;
   const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
-  cudaError_t e = encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V,
-                                (uint64_t)d * 2, kBK, BR);
-  if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
+  if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
+                    BR) != cudaSuccess)
+    return KD_ERR_UNSUPPORTED;
   // Positions go through in groups of G chunks (one GEMM launch per group:
   // more tiles per launch, fewer launches; the group is the unit the
   // workspace is sized for).
@@ -389,12 +436,13 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
     const int rows = (int)((T - c0) < gchunk ? (T - c0) : gchunk);
     {
       ProfScope ps(K_PREP, s);
-      e = launch_prep(ids + c0 * K, logp + c0 * K, rows, K, (int)V, L.Kp, ids_sorted, p_sorted, cnt, ent, status, s);
+      e = launch_prep(ids + c0 * K, logp + c0 * K, rows, K, (int)V, L.Kp, o.inv_tau, ids_sorted, p_sorted, cnt, ent,
+                      status, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
-    e = encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + c0 * d, (uint64_t)d, (uint64_t)rows,
-                      (uint64_t)d * 2, kBK, kBM);
-    if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
+    if (encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + c0 * d, (uint64_t)d, (uint64_t)rows,
+                      (uint64_t)d * 2, kBK, kBM) != cudaSuccess)
+      return KD_ERR_UNSUPPORTED;
     Problem& P = a.pr[0];
     P.m_blocks = (int)ceil_div(rows, TR);
     P.n_blocks = (int)ceil_div(V, kBNLogits);
@@ -416,47 +464,59 @@ int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const floa
     if (e != cudaSuccess) return cuda_status(e);
     {
       ProfScope ps(K_MERGE, s);
-      e = launch_merge(part_m, part_s, (int)L.S, rows, ent, p_sorted, zK, cnt, L.Kp, lse + c0,
+      e = launch_merge(part_m, part_s, (int)L.S, rows, ent, p_sorted, zK, cnt, L.Kp, mask_at(o, c0), lse + c0,
                        loss_rows ? loss_rows + c0 : nullptr, bsum, done, acc, c0 == 0, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
   }
   ProfScope ps(K_FINALIZE, s);
-  return cuda_status(launch_finalize(acc, 1.0 / (double)T, loss, s));
+  return cuda_status(launch_finalize(acc, T, o.mask, o.mean_over_mask, loss, s));
 }
 
-int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const float* logp, const float* lse,
-                    int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk, float grad_scale,
-                    const float* grad_scale_dev, float* dH, float* dW, int32_t accumulate_dW, void* ws,
+int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
+                    int64_t V, int32_t K, int64_t chunk, float* loss, float* lse, float* loss_rows, void* ws,
                     size_t ws_bytes, void* stream) {
+  return kd_fused_kl_fwd_ex(H, W, ids, logp, T, d, V, K, chunk, loss, lse, loss_rows, nullptr, ws, ws_bytes, stream);
+}
+
+int kd_fused_kl_bwd_ex(const void* H, const void* W, const int32_t* ids, const float* logp, const float* lse,
+                       int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk, float grad_scale,
+                       const float* grad_scale_dev, void* dH, float* dW, int32_t accumulate_dW,
+                       const kd_kl_options* opt, void* ws, size_t ws_bytes, void* stream) {
   int st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, ws, ws_bytes);
   if (st != KD_OK) return st;
   if (!lse || !dH || !dW) return KD_ERR_INVALID_ARG;
   if (!aligned(dH, 16) || !aligned(dW, 16)) return KD_ERR_UNSUPPORTED;
+  LossOpts o;
+  if ((st = parse_opts(opt, &o)) != KD_OK) return st;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout L = fused_layout(d, V, K, chunk);
   uint8_t* w = static_cast<uint8_t*>(ws);
   int* status = reinterpret_cast<int*>(w);
+  float* wscale = reinterpret_cast<float*>(w + kScaleOffset);
   int* ids_sorted = reinterpret_cast<int*>(w + L.ids_sorted);
   float* p_sorted = reinterpret_cast<float*>(w + L.p_sorted);
   int* cnt = reinterpret_cast<int*>(w + L.cnt);
   float* ent = reinterpret_cast<float*>(w + L.ent);
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(w + L.dz);
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
+  int* counter = reinterpret_cast<int*>(w + kCounterOffset);
+  __nv_bfloat16* hct = reinterpret_cast<__nv_bfloat16*>(w + L.hct);
 
+  // s = grad_scale * (*grad_scale_dev) * 1/tau (* 1/N), on the device.
+  cudaError_t e = launch_grad_scale(grad_scale, grad_scale_dev, o.inv_tau, o.mask, T, o.mean_over_mask, wscale, s);
+  if (e != cudaSuccess) return cuda_status(e);
   GemmArgs az, ag;
   std::memset(&az, 0, sizeof(az));
   az.cta2 = gemm_cta2();
+  az.zscale = o.inv_tau;
   const int TR = gemm_tile_rows(az.cta2), BR = gemm_b_box_rows(az.cta2);
-  int* counter = reinterpret_cast<int*>(w + kCounterOffset);
-  __nv_bfloat16* hct = reinterpret_cast<__nv_bfloat16*>(w + L.hct);
-  cudaError_t e;
   // W: K-major B of the logits GEMM, M-major A of the dH^T GEMM.
-  e = encode_map_2d(&az.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2,
-                    kBK, BR);
-  if (e != cudaSuccess) return KD_ERR_UNSUPPORTED;
+  if (encode_map_2d(&az.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
+                    BR) != cudaSuccess)
+    return KD_ERR_UNSUPPORTED;
   st = grad_setup(ag, W, dW, d, V, status, counter);
   if (st != KD_OK) return st;
 
@@ -467,7 +527,8 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
     const int grows = (int)((T - g0) < gchunk ? (T - g0) : gchunk);
     {
       ProfScope ps(K_PREP, s);
-      e = launch_prep(ids + g0 * K, logp + g0 * K, grows, K, (int)V, L.Kp, ids_sorted, p_sorted, cnt, ent, status, s);
+      e = launch_prep(ids + g0 * K, logp + g0 * K, grows, K, (int)V, L.Kp, o.inv_tau, ids_sorted, p_sorted, cnt, ent,
+                      status, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
     // Recompute the group's logits; the epilogue writes dz (bf16).
@@ -487,7 +548,8 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
       az.total_tiles = P.m_blocks * P.n_blocks;
       az.rows = grows; az.row_stride = (int)gchunk; az.V = (int)V; az.Kp = L.Kp;
       az.ids_sorted = ids_sorted; az.p_sorted = p_sorted; az.cnt = cnt;
-      az.lse = lse + g0; az.scale = grad_scale; az.dscale = grad_scale_dev;
+      az.lse = lse + g0; az.scale = 1.f; az.dscale = wscale;
+      az.mask = mask_at(o, g0);
       az.status = status;
       az.tile_counter = counter;
     }
@@ -496,20 +558,30 @@ int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const floa
       e = launch_logits_dz(az, sms, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
-    st = grad_group(ag, L, Hb, dz, hct, dH, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms, s);
+    st = grad_group(ag, L, Hb, dz, hct, dH, o.dH_bf16, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms, s);
     if (st != KD_OK) return st;
   }
   return KD_OK;
 }
 
-int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
-                       int64_t V, int32_t K, int64_t chunk, float grad_scale, const float* grad_scale_dev,
-                       float* loss, float* lse, float* loss_rows, float* dH, float* dW, int32_t accumulate_dW,
-                       void* ws, size_t ws_bytes, void* stream) {
+int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, const float* logp, const float* lse,
+                    int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk, float grad_scale,
+                    const float* grad_scale_dev, float* dH, float* dW, int32_t accumulate_dW, void* ws,
+                    size_t ws_bytes, void* stream) {
+  return kd_fused_kl_bwd_ex(H, W, ids, logp, lse, T, d, V, K, chunk, grad_scale, grad_scale_dev, dH, dW,
+                            accumulate_dW, nullptr, ws, ws_bytes, stream);
+}
+
+int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
+                          int64_t V, int32_t K, int64_t chunk, float grad_scale, const float* grad_scale_dev,
+                          float* loss, float* lse, float* loss_rows, void* dH, float* dW, int32_t accumulate_dW,
+                          const kd_kl_options* opt, void* ws, size_t ws_bytes, void* stream) {
   int st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, ws, ws_bytes);
   if (st != KD_OK) return st;
   if (!loss || !lse || !dH || !dW) return KD_ERR_INVALID_ARG;
   if (!aligned(dH, 16) || !aligned(dW, 16)) return KD_ERR_UNSUPPORTED;
+  LossOpts o;
+  if ((st = parse_opts(opt, &o)) != KD_OK) return st;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -519,6 +591,7 @@ int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, const f
   int* counter = reinterpret_cast<int*>(w + kCounterOffset);
   double* acc = reinterpret_cast<double*>(w + kAccOffset);
   unsigned* done = reinterpret_cast<unsigned*>(w + kDoneOffset);
+  float* wscale = reinterpret_cast<float*>(w + kScaleOffset);
   int* ids_sorted = reinterpret_cast<int*>(w + L.ids_sorted);
   float* p_sorted = reinterpret_cast<float*>(w + L.p_sorted);
   int* cnt = reinterpret_cast<int*>(w + L.cnt);
@@ -532,10 +605,13 @@ int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, const f
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
   cudaError_t e = cudaMemsetAsync(done, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return cuda_status(e);
+  e = launch_grad_scale(grad_scale, grad_scale_dev, o.inv_tau, o.mask, T, o.mean_over_mask, wscale, s);
+  if (e != cudaSuccess) return cuda_status(e);
 
   GemmArgs a, ag;
   std::memset(&a, 0, sizeof(a));
   a.cta2 = gemm_cta2();
+  a.zscale = o.inv_tau;
   const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
   if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
                     BR) != cudaSuccess)
@@ -544,14 +620,15 @@ int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, const f
   if (st != KD_OK) return st;
 
   // One group of G chunks at a time: the group's logits are computed once,
-  // and kept only as e = exp(z - m_tile) (bf16, in the dz buffer) until the
-  // group's lse is known.
+  // and kept only as e = exp((z - m_tile) / tau) (bf16, in the dz buffer)
+  // until the group's lse is known.
   const int64_t gchunk = L.G * chunk;
   for (int64_t g0 = 0; g0 < T; g0 += gchunk) {
     const int grows = (int)((T - g0) < gchunk ? (T - g0) : gchunk);
     {
       ProfScope ps(K_PREP, s);
-      e = launch_prep(ids + g0 * K, logp + g0 * K, grows, K, (int)V, L.Kp, ids_sorted, p_sorted, cnt, ent, status, s);
+      e = launch_prep(ids + g0 * K, logp + g0 * K, grows, K, (int)V, L.Kp, o.inv_tau, ids_sorted, p_sorted, cnt, ent,
+                      status, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
     if (encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + g0 * d, (uint64_t)d, (uint64_t)grows,
@@ -579,21 +656,29 @@ int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, const f
     if (e != cudaSuccess) return cuda_status(e);
     {
       ProfScope ps(K_MERGE, s);
-      e = launch_merge(part_m, part_s, (int)L.S, grows, ent, p_sorted, zK, cnt, L.Kp, lse + g0,
+      e = launch_merge(part_m, part_s, (int)L.S, grows, ent, p_sorted, zK, cnt, L.Kp, mask_at(o, g0), lse + g0,
                        loss_rows ? loss_rows + g0 : nullptr, bsum, done, acc, g0 == 0, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
     {
       ProfScope ps(K_DZ_FROM_EXP, s);
       e = launch_dz_from_exp(dz, L.ldz, (int)V, (int)L.S, grows, part_m, lse + g0, ids_sorted, p_sorted, zK, cnt,
-                             L.Kp, grad_scale, grad_scale_dev, s);
+                             L.Kp, 1.f, wscale, mask_at(o, g0), s);
     }
     if (e != cudaSuccess) return cuda_status(e);
-    st = grad_group(ag, L, Hb, dz, hct, dH, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms, s);
+    st = grad_group(ag, L, Hb, dz, hct, dH, o.dH_bf16, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms, s);
     if (st != KD_OK) return st;
   }
   ProfScope ps(K_FINALIZE, s);
-  return cuda_status(launch_finalize(acc, 1.0 / (double)T, loss, s));
+  return cuda_status(launch_finalize(acc, T, o.mask, o.mean_over_mask, loss, s));
+}
+
+int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
+                       int64_t V, int32_t K, int64_t chunk, float grad_scale, const float* grad_scale_dev,
+                       float* loss, float* lse, float* loss_rows, float* dH, float* dW, int32_t accumulate_dW,
+                       void* ws, size_t ws_bytes, void* stream) {
+  return kd_fused_kl_fwdbwd_ex(H, W, ids, logp, T, d, V, K, chunk, grad_scale, grad_scale_dev, loss, lse, loss_rows,
+                               dH, dW, accumulate_dW, nullptr, ws, ws_bytes, stream);
 }
 
 size_t kd_teacher_topk_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk) {
@@ -626,6 +711,7 @@ int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_t d, in
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.cta2 = gemm_cta2();
+  a.zscale = 1.f;
   const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
   if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
                     BR) != cudaSuccess)
@@ -701,6 +787,7 @@ int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, i
                            : encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, 32);
   if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return KD_ERR_UNSUPPORTED;
   a.cta2 = cta2;
+  a.zscale = 1.f;
   Problem& P = a.pr[0];
   P.m_blocks = (int)ceil_div(M, gemm_tile_rows(cta2));
   P.n_blocks = (int)ceil_div(N, kBNGrad);

@@ -426,6 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(acc * BN);
+      // The loss epilogues work on z / tau: exp arguments use zl2 = log2(e) / tau
+      // and the values they keep (tile maxima, logits at teacher ids) are
+      // scaled by zscale = 1 / tau. With tau = 1 this is the plain logit.
+      const float zscale = g.zscale, zl2 = zscale * kLog2e;
 
       if (EPI == EPI_TEACHER) {
         // Online (max, sum exp) over the tile's valid columns, 32 at a time,
@@ -482,9 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int jj = 0; jj < 32; ++jj) if (jj < lim) m = fmaxf(m, u2f(v[jj]));
           }
         }
-        // Pass 2: e = exp(z - m) summed in fp32 and stored as bf16, 64
-        // columns per TMA box (columns past V are clipped by the store).
-        const float nm = -m * kLog2e;
+        // Pass 2: e = exp((z - m) / tau) summed in fp32 and stored as bf16,
+        // 64 columns per TMA box (columns past V are clipped by the store).
+        const float nm = -m * zl2;
         float s = 0.f;
         const bool box_live = m0 + 32 * wq < g.rows;
         for (int c0 = 0; c0 < nvalid; c0 += 64) {
@@ -502,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint32_t pk[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
-              const float e0 = ex2(fmaf(u2f(v[2 * jj]), kLog2e, nm));
-              const float e1 = ex2(fmaf(u2f(v[2 * jj + 1]), kLog2e, nm));
+              const float e0 = ex2(fmaf(u2f(v[2 * jj]), zl2, nm));
+              const float e1 = ex2(fmaf(u2f(v[2 * jj + 1]), zl2, nm));
               if (2 * jj < lim) s += e0;
               if (2 * jj + 1 < lim) s += e1;
               pk[jj] = pack_bf16x2(e0, e1);
@@ -530,14 +534,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           const uint32_t val = tmem_ld1(taddr + (u - (uint32_t)n0));
           tmem_wait_ld();
           if (want == u) {
-            g.zK[(size_t)row * g.Kp + k] = u2f(val);
+            g.zK[(size_t)row * g.Kp + k] = u2f(val) * zscale;
             ++k;
             want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
           }
           u = __reduce_min_sync(0xffffffffu, want);
         }
         if (row < g.rows) {
-          g.part_m[(size_t)row * g.S + tl.nb] = m;
+          g.part_m[(size_t)row * g.S + tl.nb] = m * zscale;
           g.part_s[(size_t)row * g.S + tl.nb] = s;
         }
       } else if (EPI == EPI_FWD) {
@@ -556,16 +560,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int jj = 0; jj < 32; ++jj) if (jj < lim) cm = fmaxf(cm, u2f(v[jj]));
           }
           const float mn = fmaxf(m, cm);
-          const float nb2 = -mn * kLog2e;
+          const float nb2 = -mn * zl2;
           float acc_s = 0.f;
           if (lim >= 32) {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) acc_s += ex2(fmaf(u2f(v[jj]), kLog2e, nb2));
+            for (int jj = 0; jj < 32; ++jj) acc_s += ex2(fmaf(u2f(v[jj]), zl2, nb2));
           } else {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) if (jj < lim) acc_s += ex2(fmaf(u2f(v[jj]), kLog2e, nb2));
+            for (int jj = 0; jj < 32; ++jj) if (jj < lim) acc_s += ex2(fmaf(u2f(v[jj]), zl2, nb2));
           }
-          s = s * ex2((m - mn) * kLog2e) + acc_s;
+          s = s * ex2((m - mn) * zl2) + acc_s;
           m = mn;
         }
         // Logits at the teacher ids inside [n0, n0 + nvalid): one TMEM column
@@ -577,19 +581,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           const uint32_t val = tmem_ld1(taddr + (u - (uint32_t)n0));
           tmem_wait_ld();
           if (want == u) {
-            g.zK[(size_t)row * g.Kp + k] = u2f(val);
+            g.zK[(size_t)row * g.Kp + k] = u2f(val) * zscale;
             ++k;
             want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
           }
           u = __reduce_min_sync(0xffffffffu, want);
         }
         if (row < g.rows) {
-          g.part_m[(size_t)row * g.S + tl.nb] = m;
+          g.part_m[(size_t)row * g.S + tl.nb] = m * zscale;
           g.part_s[(size_t)row * g.S + tl.nb] = s;
         }
       } else if (EPI == EPI_DZ) {
         const float lse_r = (row < g.rows) ? __ldg(g.lse + row) : 0.f;
-        const float sc = g.scale * (g.dscale ? __ldg(g.dscale) : 1.f);
+        const bool excluded = g.mask && row < g.rows && g.mask[row] == 0;
+        const float sc = excluded ? 0.f : g.scale * (g.dscale ? __ldg(g.dscale) : 1.f);
         const float nl = -lse_r * kLog2e;
         const bool box_live = m0 + 32 * wq < g.rows;
         for (int c0 = 0; c0 < nvalid; c0 += 64) {
@@ -606,8 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint32_t pk[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
-              const float e0 = ex2(fmaf(u2f(v[2 * jj]), kLog2e, nl)) * sc;
-              const float e1 = ex2(fmaf(u2f(v[2 * jj + 1]), kLog2e, nl)) * sc;
+              const float e0 = ex2(fmaf(u2f(v[2 * jj]), zl2, nl)) * sc;
+              const float e1 = ex2(fmaf(u2f(v[2 * jj + 1]), zl2, nl)) * sc;
               pk[jj] = pack_bf16x2(e0, e1);
             }
 #pragma unroll
@@ -625,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const uint32_t val = tmem_ld1(taddr + (u - (uint32_t)n0));
             tmem_wait_ld();
             if (want == u) {
-              const float q = ex2(fmaf(u2f(val), kLog2e, nl));
+              const float q = ex2(fmaf(u2f(val), zl2, nl));
               const float dz = sc * (q - __ldg(g.p_sorted + (size_t)row * g.Kp + k));
               const int jj = (int)(u - (uint32_t)n0) - c0;
               const __nv_bfloat16 hb = __float2bfloat16_rn(dz);
@@ -639,6 +644,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, n0 + c0, m0 + 32 * wq);
+          if (lane == 0) bulk_commit();
+          ++nstore;
+          buf ^= 1;
+        }
+      } else if (P.c_trans && P.out_bf16) {
+        // C^T in bf16: each warp stages 32 C rows x 32 C columns as 64-byte
+        // rows (2 bytes per lane per row; a warp's 32 lanes fill one row, so
+        // the stores are conflict-free) and stores them with one
+        // non-swizzled TMA box.
+        const CUtensorMap* mC = &g.tmC[tl.prob];
+        const bool box_live = m0 + 32 * wq < P.M;
+        for (int c0 = 0; c0 < BN && n0 + c0 < P.N; c0 += 32) {
+          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
+          if (nstore >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+          uint32_t v[32];
+          tmem_ld32(taddr + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int r = 0; r < 32; ++r) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(u2f(v[r]));
+            st_shared_u16(sb + r * 64 + lane * 2, *reinterpret_cast<const uint16_t*>(&h));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && box_live) tma_store_2d(mC, sb, m0 + 32 * wq, n0 + c0);
           if (lane == 0) bulk_commit();
           ++nstore;
           buf ^= 1;

@@ -25,6 +25,7 @@ struct Problem {
   int n_fastest;    // tile order: 1 = consecutive tiles walk N, 0 = walk M
   int reduce_add;   // fp32 epilogue: 1 = TMA reduce-add into C, 0 = store
   int c_trans;      // fp32 epilogue: 1 = write C^T (TMEM lanes are C's columns)
+  int out_bf16;     // transposed epilogue: 1 = C is bf16 (64-byte boxes, no swizzle), 0 = fp32
 };
 
 // Kernel parameters (passed as __grid_constant__; tensor maps live in param space).
@@ -51,6 +52,8 @@ struct GemmArgs {
   const float* lse;       // [rows] chunk slice of the saved log-sum-exp
   float scale;            // dz scale
   const float* dscale;    // optional device multiplier of `scale`
+  float zscale;           // logit scale 1/tau (temperature) in the loss epilogues; 1 = none
+  const uint8_t* mask;    // [rows] chunk slice of the position mask (0 = excluded), or null
   int* status;            // device status word
   int cta2;               // 1: cluster-pair tiles (256 rows, tcgen05 cta_group::2)
 };
@@ -62,6 +65,9 @@ inline int gemm_b_box_rows(int cta2) { return cta2 ? kBNLogits / 2 : kBNLogits; 
 
 cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                           uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// Same, without shared-memory swizzle (box rows land densely in smem).
+cudaError_t encode_map_2d_plain(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                                uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 
 // Launchers (kd_gemm.cu).
 cudaError_t launch_logits_fwd(const GemmArgs& a, int num_sms, cudaStream_t s);
@@ -71,16 +77,25 @@ cudaError_t launch_logits_teacher(const GemmArgs& a, int num_sms, cudaStream_t s
 cudaError_t launch_grad(const GemmArgs& a, int num_sms, cudaStream_t s);
 
 // Small kernels (kd_loss_aux.cu).
-cudaError_t launch_prep(const int32_t* ids, const float* logp, int rows, int K, int V, int Kp, int* ids_sorted,
-                        float* p_sorted, int* cnt, float* ent, int* status, cudaStream_t s);
+cudaError_t launch_prep(const int32_t* ids, const float* logp, int rows, int K, int V, int Kp, float inv_tau,
+                        int* ids_sorted, float* p_sorted, int* cnt, float* ent, int* status, cudaStream_t s);
 cudaError_t launch_merge(const float* part_m, const float* part_s, int S, int rows, const float* ent,
-                         const float* p_sorted, const float* zK, const int* cnt, int Kp, float* lse_out,
-                         float* loss_rows_out, double* block_sums, unsigned* done, double* acc, int first,
-                         cudaStream_t s);
+                         const float* p_sorted, const float* zK, const int* cnt, int Kp, const uint8_t* mask,
+                         float* lse_out, float* loss_rows_out, double* block_sums, unsigned* done, double* acc,
+                         int first, cudaStream_t s);
+// Per-position gradient factor s = grad_scale * (*grad_scale_dev, if any) *
+// inv_tau * (mean_over_mask ? 1/N : 1), N = positions with mask != 0 (0 if
+// N = 0), written to *out on the device.
+cudaError_t launch_grad_scale(float grad_scale, const float* grad_scale_dev, float inv_tau, const uint8_t* mask,
+                              int64_t T, int mean_over_mask, float* out, cudaStream_t s);
 cudaError_t launch_dz_from_exp(__nv_bfloat16* E, int64_t ldz, int V, int S, int rows, const float* part_m,
                                const float* lse, const int* ids_sorted, const float* p_sorted, const float* zK,
-                               const int* cnt, int Kp, float scale, const float* dscale, cudaStream_t s);
-cudaError_t launch_finalize(const double* acc, double inv_T, float* loss, cudaStream_t s);
+                               const int* cnt, int Kp, float scale, const float* dscale, const uint8_t* mask,
+                               cudaStream_t s);
+// loss = acc / T, or acc / N over the mask's included positions when
+// mean_over_mask (0 when N = 0).
+cudaError_t launch_finalize(const double* acc, int64_t T, const uint8_t* mask, int mean_over_mask, float* loss,
+                            cudaStream_t s);
 cudaError_t launch_transpose(const void* src, int rows, int cols, void* dst, int ld_dst, cudaStream_t s);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 

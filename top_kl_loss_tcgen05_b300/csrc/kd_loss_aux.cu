@@ -57,7 +57,8 @@ __device__ float block_reduce_sum(float v, float* sm) {
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* __restrict__ ids,
                                                             const float* __restrict__ logp, int K, int V,
-                                                            int Kp, int Kpow2, int* __restrict__ ids_sorted,
+                                                            int Kp, int Kpow2, float inv_tau,
+                                                            int* __restrict__ ids_sorted,
                                                             float* __restrict__ p_sorted, int* __restrict__ cnt,
                                                             float* __restrict__ ent, int* status) {
   extern __shared__ uint64_t keys[];  // [Kpow2]
@@ -67,17 +68,18 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* __res
   const int32_t* rid = ids + (size_t)r * K;
   const float* rl = logp + (size_t)r * K;
 
-  // Teacher renormalised over its K entries.
+  // Teacher (log-probs divided by the temperature) renormalised over its K
+  // entries.
   float mx = -INFINITY;
-  for (int k = tid; k < K; k += kPrepThreads) mx = fmaxf(mx, rl[k]);
+  for (int k = tid; k < K; k += kPrepThreads) mx = fmaxf(mx, rl[k] * inv_tau);
   mx = block_reduce_max(mx, red);
   float se = 0.f;
-  for (int k = tid; k < K; k += kPrepThreads) se += expf(rl[k] - mx);
+  for (int k = tid; k < K; k += kPrepThreads) se += expf(rl[k] * inv_tau - mx);
   se = block_reduce_sum(se, red);
   const float lse_k = mx + logf(se);
   float e = 0.f;
   for (int k = tid; k < K; k += kPrepThreads) {
-    const float lp = rl[k] - lse_k;
+    const float lp = rl[k] * inv_tau - lse_k;
     e += expf(lp) * lp;
   }
   e = block_reduce_sum(e, red);
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* __res
       const int slot = base_out + scan_w[w] + __popc(bal & ((1u << lane) - 1u));
       float ps = 0.f;
       for (int j = i; j < Kpow2 && keys[j] != kDropKey && (uint32_t)(keys[j] >> 32) == id; ++j)
-        ps += expf(rl[(uint32_t)keys[j]] - lse_k);
+        ps += expf(rl[(uint32_t)keys[j]] * inv_tau - lse_k);
       ids_sorted[(size_t)r * Kp + slot] = (int)id;
       p_sorted[(size_t)r * Kp + slot] = ps;
     }
@@ -163,7 +165,7 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 __global__ void __launch_bounds__(32 * kPrepWarpRows) prep_warp_kernel(
-    const int32_t* __restrict__ ids, const float* __restrict__ logp, int rows, int K, int V, int Kp,
+    const int32_t* __restrict__ ids, const float* __restrict__ logp, int rows, int K, int V, int Kp, float inv_tau,
     int* __restrict__ ids_sorted, float* __restrict__ p_sorted, int* __restrict__ cnt, float* __restrict__ ent,
     int* status) {
   __shared__ uint64_t skeys[kPrepWarpRows][kPrepWarpK];
@@ -182,7 +184,7 @@ __global__ void __launch_bounds__(32 * kPrepWarpRows) prep_warp_kernel(
     lv[q] = -INFINITY;
     key[q] = kDropKey;
     if (i < K) {
-      lv[q] = __ldg(rl + i);
+      lv[q] = __ldg(rl + i) * inv_tau;
       const int id = __ldg(rid + i);
       if (id < 0 || id >= V) bad = true;
       else key[q] = ((uint64_t)(uint32_t)id << 32) | (uint32_t)i;
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(32 * kPrepWarpRows) prep_warp_kernel(
     const uint32_t id = (uint32_t)(key[q] >> 32);
     float ps = 0.f;
     for (int j = pos; j < kPrepWarpK && skeys[w][j] != kDropKey && (uint32_t)(skeys[w][j] >> 32) == id; ++j)
-      ps += expf(__ldg(rl + (uint32_t)skeys[w][j]) - lse_k);
+      ps += expf(__ldg(rl + (uint32_t)skeys[w][j]) * inv_tau - lse_k);
     ids_sorted[(size_t)r * Kp + slot] = (int)id;
     p_sorted[(size_t)r * Kp + slot] = ps;
     ++slot;
@@ -286,7 +288,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
                                                     const float* __restrict__ ent,
                                                     const float* __restrict__ p_sorted,
                                                     const float* __restrict__ zK, const int* __restrict__ cnt,
-                                                    int Kp, float* __restrict__ lse_out,
+                                                    int Kp, const uint8_t* __restrict__ mask,
+                                                    float* __restrict__ lse_out,
                                                     float* __restrict__ loss_rows_out,
                                                     double* __restrict__ block_sums, unsigned* done,
                                                     double* acc, int first) {
@@ -318,6 +321,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
     L = ent[row] - dot + lse;
+    if (mask && mask[row] == 0) L = 0.f;  // excluded position
     if (lane == 0) {
       lse_out[row] = lse;
       if (loss_rows_out) loss_rows_out[row] = L;
@@ -353,8 +357,49 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
   }
 }
 
-__global__ void finalize_kernel(const double* acc, double inv_T, float* loss) {
-  if (threadIdx.x == 0 && blockIdx.x == 0) *loss = (float)(*acc * inv_T);
+// loss = acc / T, or acc / N (N = included positions, counted here in a
+// fixed order) when mean_over_mask.
+__global__ void __launch_bounds__(256) finalize_kernel(const double* acc, int64_t T, const uint8_t* mask,
+                                                       int mean_over_mask, float* loss) {
+  __shared__ long long part[8];
+  if (!(mask && mean_over_mask)) {
+    if (threadIdx.x == 0) *loss = (float)(*acc / (double)T);
+    return;
+  }
+  long long n = 0;
+  for (int64_t t = threadIdx.x; t < T; t += blockDim.x) n += mask[t] != 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = n;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long tot = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += part[i];
+    *loss = tot > 0 ? (float)(*acc / (double)tot) : 0.f;
+  }
+}
+
+// The backward's per-position gradient factor (see launch_grad_scale).
+__global__ void __launch_bounds__(256) grad_scale_kernel(float grad_scale, const float* grad_scale_dev,
+                                                         float inv_tau, const uint8_t* mask, int64_t T,
+                                                         int mean_over_mask, float* out) {
+  __shared__ long long part[8];
+  long long n = 0;
+  if (mask && mean_over_mask)
+    for (int64_t t = threadIdx.x; t < T; t += blockDim.x) n += mask[t] != 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = n;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = grad_scale * (grad_scale_dev ? *grad_scale_dev : 1.f) * inv_tau;
+    if (mask && mean_over_mask) {
+      long long tot = 0;
+      for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += part[i];
+      s = tot > 0 ? s / (float)tot : 0.f;
+    }
+    *out = s;
+  }
 }
 
 // dst[c][r] = src[r][c] for a bf16 [rows, cols] matrix (dst row stride
@@ -404,9 +449,10 @@ __global__ void __launch_bounds__(kDzThreads) dz_from_exp_kernel(uint16_t* __res
                                                                 const float* __restrict__ p_sorted,
                                                                 const float* __restrict__ zK,
                                                                 const int* __restrict__ cnt, int Kp, float scale,
-                                                                const float* __restrict__ dscale) {
+                                                                const float* __restrict__ dscale,
+                                                                const uint8_t* __restrict__ mask) {
   const int r = blockIdx.x;
-  const float sc = scale * (dscale ? __ldg(dscale) : 1.f);
+  const float sc = scale * (dscale ? __ldg(dscale) : 1.f) * ((mask && mask[r] == 0) ? 0.f : 1.f);
   const float l2 = __ldg(lse + r) * kLog2e;
   uint16_t* row = E + (size_t)r * ldz;
   const float* pm = part_m + (size_t)r * S;
@@ -441,10 +487,11 @@ __global__ void __launch_bounds__(kDzThreads) dz_from_exp_kernel(uint16_t* __res
 
 cudaError_t launch_dz_from_exp(__nv_bfloat16* E, int64_t ldz, int V, int S, int rows, const float* part_m,
                                const float* lse, const int* ids_sorted, const float* p_sorted, const float* zK,
-                               const int* cnt, int Kp, float scale, const float* dscale, cudaStream_t s) {
+                               const int* cnt, int Kp, float scale, const float* dscale, const uint8_t* mask,
+                               cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   dz_from_exp_kernel<<<rows, kDzThreads, 0, s>>>(reinterpret_cast<uint16_t*>(E), ldz, V, S, part_m, lse, ids_sorted,
-                                                p_sorted, zK, cnt, Kp, scale, dscale);
+                                                p_sorted, zK, cnt, Kp, scale, dscale, mask);
   return cudaGetLastError();
 }
 
@@ -460,12 +507,12 @@ cudaError_t launch_transpose(const void* src, int rows, int cols, void* dst, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_prep(const int32_t* ids, const float* logp, int rows, int K, int V, int Kp, int* ids_sorted,
-                        float* p_sorted, int* cnt, float* ent, int* status, cudaStream_t s) {
+cudaError_t launch_prep(const int32_t* ids, const float* logp, int rows, int K, int V, int Kp, float inv_tau,
+                        int* ids_sorted, float* p_sorted, int* cnt, float* ent, int* status, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (K <= kPrepWarpK) {
     prep_warp_kernel<<<(rows + kPrepWarpRows - 1) / kPrepWarpRows, 32 * kPrepWarpRows, 0, s>>>(
-        ids, logp, rows, K, V, Kp, ids_sorted, p_sorted, cnt, ent, status);
+        ids, logp, rows, K, V, Kp, inv_tau, ids_sorted, p_sorted, cnt, ent, status);
     return cudaGetLastError();
   }
   int Kpow2 = 1;
@@ -476,23 +523,30 @@ cudaError_t launch_prep(const int32_t* ids, const float* logp, int rows, int K, 
     cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  prep_kernel<<<rows, kPrepThreads, smem, s>>>(ids, logp, K, V, Kp, Kpow2, ids_sorted, p_sorted, cnt, ent,
-                                              status);
+  prep_kernel<<<rows, kPrepThreads, smem, s>>>(ids, logp, K, V, Kp, Kpow2, inv_tau, ids_sorted, p_sorted, cnt,
+                                              ent, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_merge(const float* part_m, const float* part_s, int S, int rows, const float* ent,
-                         const float* p_sorted, const float* zK, const int* cnt, int Kp, float* lse_out,
-                         float* loss_rows_out, double* block_sums, unsigned* done, double* acc, int first,
-                         cudaStream_t s) {
+                         const float* p_sorted, const float* zK, const int* cnt, int Kp, const uint8_t* mask,
+                         float* lse_out, float* loss_rows_out, double* block_sums, unsigned* done, double* acc,
+                         int first, cudaStream_t s) {
   const int nb = (rows + 7) / 8;
-  merge_kernel<<<nb, 256, 0, s>>>(part_m, part_s, S, rows, ent, p_sorted, zK, cnt, Kp, lse_out, loss_rows_out,
+  merge_kernel<<<nb, 256, 0, s>>>(part_m, part_s, S, rows, ent, p_sorted, zK, cnt, Kp, mask, lse_out, loss_rows_out,
                                   block_sums, done, acc, first);
   return cudaGetLastError();
 }
 
-cudaError_t launch_finalize(const double* acc, double inv_T, float* loss, cudaStream_t s) {
-  finalize_kernel<<<1, 32, 0, s>>>(acc, inv_T, loss);
+cudaError_t launch_finalize(const double* acc, int64_t T, const uint8_t* mask, int mean_over_mask, float* loss,
+                            cudaStream_t s) {
+  finalize_kernel<<<1, 256, 0, s>>>(acc, T, mask, mean_over_mask, loss);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grad_scale(float grad_scale, const float* grad_scale_dev, float inv_tau, const uint8_t* mask,
+                              int64_t T, int mean_over_mask, float* out, cudaStream_t s) {
+  grad_scale_kernel<<<1, 256, 0, s>>>(grad_scale, grad_scale_dev, inv_tau, mask, T, mean_over_mask, out);
   return cudaGetLastError();
 }
 
