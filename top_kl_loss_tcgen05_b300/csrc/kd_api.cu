@@ -150,12 +150,12 @@ TeacherLayout teacher_layout(int64_t V, int64_t chunk) {
 // Kernel names reported by kd_profile_end, indexed by KernelId.
 enum KernelId {
   K_TOPK, K_PREP, K_LOGITS_FWD, K_MERGE, K_FINALIZE, K_LOGITS_DZ, K_TRANSPOSE, K_GRAD, K_TEST, K_LOGITS_FWD_STORE,
-  K_DZ_FROM_EXP, K_TEACHER_GEMM, K_TILE_TOPK, K_COUNT
+  K_DZ_FROM_EXP, K_TEACHER_GEMM, K_TILE_TOPK, K_GRAD_SCALE, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {"topk_cache", "teacher_prep", "logits_fwd_lse_gather", "lse_merge_loss",
                                            "loss_finalize", "logits_dz", "hidden_transpose", "grad_dH_dW",
                                            "test_gemm", "logits_fwd_store_exp", "dz_from_exp",
-                                           "teacher_logits_gemm", "teacher_tile_topk"};
+                                           "teacher_logits_gemm", "teacher_tile_topk", "grad_scale"};
 struct ProfRec {
   int kid;
   cudaEvent_t a, b;
@@ -506,7 +506,11 @@ int kd_fused_kl_bwd_ex(const void* H, const void* W, const int32_t* ids, const f
   __nv_bfloat16* hct = reinterpret_cast<__nv_bfloat16*>(w + L.hct);
 
   // s = grad_scale * (*grad_scale_dev) * 1/tau (* 1/N), on the device.
-  cudaError_t e = launch_grad_scale(grad_scale, grad_scale_dev, o.inv_tau, o.mask, T, o.mean_over_mask, wscale, s);
+  cudaError_t e;
+  {
+    ProfScope ps(K_GRAD_SCALE, s);
+    e = launch_grad_scale(grad_scale, grad_scale_dev, o.inv_tau, o.mask, T, o.mean_over_mask, wscale, s);
+  }
   if (e != cudaSuccess) return cuda_status(e);
   GemmArgs az, ag;
   std::memset(&az, 0, sizeof(az));
@@ -605,7 +609,10 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
   cudaError_t e = cudaMemsetAsync(done, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return cuda_status(e);
-  e = launch_grad_scale(grad_scale, grad_scale_dev, o.inv_tau, o.mask, T, o.mean_over_mask, wscale, s);
+  {
+    ProfScope ps(K_GRAD_SCALE, s);
+    e = launch_grad_scale(grad_scale, grad_scale_dev, o.inv_tau, o.mask, T, o.mean_over_mask, wscale, s);
+  }
   if (e != cudaSuccess) return cuda_status(e);
 
   GemmArgs a, ag;
