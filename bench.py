@@ -204,10 +204,21 @@ def cpu_workload(wl):
                 logp=wl["logp"][:4096].cpu().numpy())
 
 
+def size_sample(cw, budget_s: float) -> int:
+    """Rows of oracle work that take about budget_s: time(r) = a + b r is
+    fitted from 2 and 8 rows after a warm-up call (a is the per-call cost,
+    e.g. allocating the fp64 dW)."""
+    oracle_sample(cw, 2)
+    t2 = oracle_sample(cw, 2)
+    t8 = oracle_sample(cw, 8)
+    b = max((t8 - t2) / 6.0, 1e-6)
+    a = max(t2 - 2.0 * b, 0.0)
+    return int(max(2, min(len(cw["ids"]), (budget_s - a) / b)))
+
+
 def cpu_baseline(wl, budget_s: float = 15.0):
     cw = cpu_workload(wl)
-    t1 = oracle_sample(cw, 2)
-    rows = int(max(2, min(4096, budget_s / max(t1 / 2, 1e-6))))
+    rows = size_sample(cw, budget_s)
     t = oracle_sample(cw, rows)
     return {"value": rows / t, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
             "sample": "fp64 numpy oracle, forward + backward (loss, lse, dH, dW contribution) of the first %d "
@@ -344,10 +355,11 @@ def run_reference(args, world, rank):
     ids, logp = synth.synthetic_cache(min(c["T"], 4096), c["V"], c["K"], c["seed"])
     cw = dict(T=c["T"], H=H.float().numpy().astype(np.float64), W64=W.float().numpy().astype(np.float64),
               ids=ids.numpy(), logp=logp.numpy())
-    t1 = oracle_sample(cw, 2)
-    rows = int(max(2, min(4096, 8.0 / max(t1 / 2, 1e-6))))
+    # each step a bounded sample, sized so the whole run takes about 2.5 min
+    per_step = max(1.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows = size_sample(cw, per_step)
     for _ in range(args.warmup):
-        oracle_sample(cw, 2)
+        oracle_sample(cw, rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         oracle_sample(cw, rows)
