@@ -487,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 5) topk_kernel(const Tin* __restrict
 
 constexpr int kTileW = kBNLogits;     // columns per tile of the teacher GEMM
 constexpr int kTileListCap = 1024;    // tiles at or above tau read by the fast path
+constexpr int kTauKeysPerLane = 32;   // warp-held tile-maximum keys (up to 1024 tiles)
 
 __device__ __forceinline__ float block_max_f(float v, float* red) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -524,7 +525,7 @@ __device__ __forceinline__ int block_sum_i(int v, int* red) {
 }
 
 // One block per row of the chunk.
-__global__ void __launch_bounds__(kThreads) tile_topk_kernel(const float* __restrict__ Z, int64_t ldz, int V, int S,
+__global__ void __launch_bounds__(kThreads, 4) tile_topk_kernel(const float* __restrict__ Z, int64_t ldz, int V, int S,
                                                             const float* __restrict__ part_m,
                                                             const float* __restrict__ part_s, int K,
                                                             int force_exact, int32_t* __restrict__ ids,
@@ -538,6 +539,7 @@ __global__ void __launch_bounds__(kThreads) tile_topk_kernel(const float* __rest
   __shared__ int sm_ired[kWarps];
   __shared__ int tiles[kTileListCap];
   __shared__ int sm_nt, sm_n;
+  __shared__ uint32_t sm_tau;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;
   const float* pm = part_m + (size_t)row * S;
@@ -555,9 +557,31 @@ __global__ void __launch_bounds__(kThreads) tile_topk_kernel(const float* __rest
 
   bool exact = force_exact || K > kFastMaxK;
   if (!exact) {
-    // tau: the K-th largest tile maximum (key 0 = take every tile)
+    // tau: the K-th largest tile maximum (key 0 = take every tile), by
+    // bisection on the order keys. Up to 1024 tiles (V <= 262144), one warp
+    // holds every key in registers and counts with warp reductions, so the
+    // block waits at a single barrier; larger rows count block-wide.
     uint32_t kth = 0;
-    if (S > K) {
+    if (S > K && S <= 32 * kTauKeysPerLane) {
+      if (warp == 0) {
+        uint32_t key[kTauKeysPerLane];
+#pragma unroll
+        for (int i = 0; i < kTauKeysPerLane; ++i) {
+          const int j = lane + 32 * i;
+          key[i] = j < S ? okey(__ldg(pm + j)) : 0u;  // key 0 never reaches c >= 1
+        }
+        for (int b = 31; b >= 0; --b) {
+          const uint32_t c = kth | (1u << b);
+          uint32_t cnt = 0;
+#pragma unroll
+          for (int i = 0; i < kTauKeysPerLane; ++i) cnt += key[i] >= c;
+          if ((int)__reduce_add_sync(0xffffffffu, cnt) >= K) kth = c;
+        }
+        if (lane == 0) sm_tau = kth;
+      }
+      __syncthreads();
+      kth = sm_tau;
+    } else if (S > K) {
       for (int b = 31; b >= 0; --b) {
         const uint32_t c = kth | (1u << b);
         int cnt = 0;
@@ -578,23 +602,34 @@ __global__ void __launch_bounds__(kThreads) tile_topk_kernel(const float* __rest
     if (nt > kTileListCap) {
       exact = true;
     } else {
-      // a warp per listed tile: 32 lanes x 8 consecutive columns
-      for (int i = warp; i < nt; i += kWarps) {
-        const int c0 = tiles[i] * kTileW + lane * 8;
-        float x[8];
-        if (c0 + 8 <= V) {
-          const float4 a = __ldg(reinterpret_cast<const float4*>(zr + c0));
-          const float4 b = __ldg(reinterpret_cast<const float4*>(zr + c0 + 4));
-          x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-        } else {
+      // a warp per listed tile (32 lanes x 8 consecutive columns), four
+      // tiles' loads in flight per warp before any is processed
+      constexpr int kTilesInFlight = 4;
+      for (int i0 = warp; i0 < nt; i0 += kWarps * kTilesInFlight) {
+        float x[kTilesInFlight][8];
+        int c0[kTilesInFlight];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) x[j] = c0 + j < V ? __ldg(zr + c0 + j) : -INFINITY;
+        for (int u = 0; u < kTilesInFlight; ++u) {
+          const int i = i0 + u * kWarps;
+          c0[u] = i < nt ? tiles[i] * kTileW + lane * 8 : V;  // V: nothing to read
+          if (c0[u] + 8 <= V) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(zr + c0[u]));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(zr + c0[u] + 4));
+            x[u][0] = a.x; x[u][1] = a.y; x[u][2] = a.z; x[u][3] = a.w;
+            x[u][4] = b.x; x[u][5] = b.y; x[u][6] = b.z; x[u][7] = b.w;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[u][j] = c0[u] + j < V ? __ldg(zr + c0[u] + j) : -INFINITY;
+          }
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (c0 + j < V && okey(x[j]) >= kth) {
-            const int p = atomicAdd(&sm_n, 1);
-            if (p < kCandCap) cand[p] = rkey(x[j], (uint32_t)(c0 + j));
+        for (int u = 0; u < kTilesInFlight; ++u) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (c0[u] + j < V && okey(x[u][j]) >= kth) {
+              const int p = atomicAdd(&sm_n, 1);
+              if (p < kCandCap) cand[p] = rkey(x[u][j], (uint32_t)(c0[u] + j));
+            }
           }
         }
       }
