@@ -22,6 +22,8 @@ extern "C" {
  *   flags bit 1: store C transposed, i.e. C is [N, M] row-major.
  *   flags bit 2: CTA-pair tiles (256 x 256 per cluster of two CTAs, tcgen05
  *                cta_group::2); needs b_mn == 0 (else KD_ERR_UNSUPPORTED).
+ *   flags bit 3: with bit 2, wide pair tiles (256 x 512, one 512-column
+ *                accumulator, eight epilogue warps).
  * Requires K, and M or N for MN-major operands, to be multiples of 8, and
  * C's row length a multiple of 4. `ws` (>= 256 bytes, device) holds the
  * status word and the tile counter. Returns a kd_status value. */

@@ -20,10 +20,17 @@ LOSS_RTOL = 1e-3
 GRAD_RTOL = 1e-2
 
 
-@pytest.fixture(params=["0", "1"], ids=["cta1", "cta2"], autouse=True)
+@pytest.fixture(params=[("0", None), ("1", None), ("1", "0"), ("1", "1")],
+                ids=["cta1", "cta2", "cta2-narrow", "cta2-wide"], autouse=True)
 def gemm_tiles(request, monkeypatch):
-    """Every test runs with one CTA per GEMM tile and with CTA-pair tiles."""
-    monkeypatch.setenv("KD_GEMM_CTA2", request.param)
+    """Every test runs with one CTA per GEMM tile, with CTA-pair tiles at the
+    per-kernel default widths, and with every pair GEMM narrow or wide."""
+    cta2, wide = request.param
+    monkeypatch.setenv("KD_GEMM_CTA2", cta2)
+    if wide is None:
+        monkeypatch.delenv("KD_GEMM_WIDE", raising=False)
+    else:
+        monkeypatch.setenv("KD_GEMM_WIDE", wide)
     return request.param
 
 

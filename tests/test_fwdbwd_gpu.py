@@ -22,9 +22,17 @@ LOSS_RTOL = 1e-3
 GRAD_RTOL = 1e-2
 
 
-@pytest.fixture(params=["0", "1"], ids=["cta1", "cta2"], autouse=True)
+@pytest.fixture(params=[("0", None), ("1", None), ("1", "0"), ("1", "1")],
+                ids=["cta1", "cta2", "cta2-narrow", "cta2-wide"], autouse=True)
 def gemm_tiles(request, monkeypatch):
-    monkeypatch.setenv("KD_GEMM_CTA2", request.param)
+    """Every test runs with one CTA per GEMM tile, with CTA-pair tiles at the
+    per-kernel default widths, and with every pair GEMM narrow or wide."""
+    cta2, wide = request.param
+    monkeypatch.setenv("KD_GEMM_CTA2", cta2)
+    if wide is None:
+        monkeypatch.delenv("KD_GEMM_WIDE", raising=False)
+    else:
+        monkeypatch.setenv("KD_GEMM_WIDE", wide)
     return request.param
 
 
@@ -142,8 +150,8 @@ def test_grad_scale_and_accumulate(cuda_dev):
 def test_full_width_truncated_run(cuda_dev, gemm_tiles, name):
     """Full d, V and chunk of the workloads, T = 2 chunks + a ragged tail of
     37: every element of dW and dH against the oracle."""
-    if gemm_tiles == "0":
-        pytest.skip("full-width check runs in the default tile mode")
+    if gemm_tiles != ("1", None):
+        pytest.skip("full-width check runs in the default tile configuration")
     c = synth.CONFIGS[name]
     chunk = c["chunk"]
     Tp = 2 * chunk + 37

@@ -2,7 +2,7 @@
 store / reduce-add) against a plain PyTorch fp64 product of the same bf16
 operands, for every operand layout the backward pass uses and ragged edges in
 M, N and K, with one CTA per 128 x 256 tile and with CTA-pair 256 x 256 tiles
-(tcgen05 cta_group::2)."""
+(tcgen05 cta_group::2) both 256 x 256 and 256 x 512 wide."""
 
 import pytest
 import torch
@@ -12,7 +12,7 @@ from top_kl_loss_tcgen05_b300 import _native, workspace
 pytestmark = pytest.mark.gpu
 
 
-def _run(M, N, K, a_mn, b_mn, reduce_add=False, seed=0, c_trans=False, pair=False):
+def _run(M, N, K, a_mn, b_mn, reduce_add=False, seed=0, c_trans=False, pair=False, wide=False):
     dev = torch.device("cuda:0")
     g = torch.Generator(device=dev).manual_seed(seed)
     A = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
@@ -23,7 +23,7 @@ def _run(M, N, K, a_mn, b_mn, reduce_add=False, seed=0, c_trans=False, pair=Fals
     C0 = torch.randn(*shape, generator=g, device=dev) if reduce_add else torch.full(shape, float("nan"), device=dev)
     C = C0.clone()
     ws = workspace(256, dev)
-    flags = (1 if reduce_add else 0) | (2 if c_trans else 0) | (4 if pair else 0)
+    flags = (1 if reduce_add else 0) | (2 if c_trans else 0) | (4 if pair else 0) | (8 if wide else 0)
     rc = _native.lib().kd_test_gemm(Ain.data_ptr(), Bin.data_ptr(), C.data_ptr(), M, N, K, a_mn, b_mn,
                                     flags, ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert rc == 0, _native.status_string(rc)
@@ -70,25 +70,29 @@ def test_gemm_transposed_reduce_add(cuda_dev):
     _run(136, 520, 64, 1, 0, reduce_add=True, seed=7, c_trans=True)
 
 
-# CTA-pair tiles: B is K-major (as for every GEMM of the loss).
+# CTA-pair tiles (256 x 256, and wide 256 x 512): B is K-major.
+@pytest.mark.parametrize("wide", [False, True], ids=["pair", "wide"])
 @pytest.mark.parametrize("a_mn", [0, 1])
-def test_pair_tiles_layouts(cuda_dev, a_mn):
-    _run(256, 512, 256, a_mn, 0, pair=True)
-    _run(136, 200, 72, a_mn, 0, seed=1, pair=True)       # one pair tile, both halves ragged
-    _run(1000, 584, 1032, a_mn, 0, seed=2, pair=True)
-    _run(64, 1000, 128, a_mn, 0, seed=8, pair=True)      # odd CTA's rows all out of range
+def test_pair_tiles_layouts(cuda_dev, a_mn, wide):
+    _run(256, 512, 256, a_mn, 0, pair=True, wide=wide)
+    _run(136, 200, 72, a_mn, 0, seed=1, pair=True, wide=wide)       # one tile, every part ragged
+    _run(1000, 584, 1032, a_mn, 0, seed=2, pair=True, wide=wide)    # second N half partly past N
+    _run(64, 1000, 128, a_mn, 0, seed=8, pair=True, wide=wide)      # odd CTA's rows all out of range
+    _run(296, 248, 64, a_mn, 0, seed=10, pair=True, wide=wide)      # wide: second half entirely past N
 
 
-def test_pair_tiles_many_tiles_and_reduce_add(cuda_dev):
-    _run(256 * 30, 256 * 11, 192, 0, 0, seed=9, pair=True)   # several tiles per CTA pair
-    _run(520, 392, 200, 1, 0, reduce_add=True, seed=3, pair=True)
+@pytest.mark.parametrize("wide", [False, True], ids=["pair", "wide"])
+def test_pair_tiles_many_tiles_and_reduce_add(cuda_dev, wide):
+    _run(256 * 30, 256 * 11, 192, 0, 0, seed=9, pair=True, wide=wide)   # several tiles per CTA pair
+    _run(520, 392, 200, 1, 0, reduce_add=True, seed=3, pair=True, wide=wide)
 
 
+@pytest.mark.parametrize("wide", [False, True], ids=["pair", "wide"])
 @pytest.mark.parametrize("a_mn", [0, 1])
-def test_pair_tiles_transposed_store(cuda_dev, a_mn):
-    _run(264, 1000, 520, a_mn, 0, seed=5, c_trans=True, pair=True)
-    _run(3072, 1024, 4096, a_mn, 0, seed=6, c_trans=True, pair=True)
-    _run(136, 520, 64, 1, 0, reduce_add=True, seed=7, c_trans=True, pair=True)
+def test_pair_tiles_transposed_store(cuda_dev, a_mn, wide):
+    _run(264, 1000, 520, a_mn, 0, seed=5, c_trans=True, pair=True, wide=wide)
+    _run(3072, 1024, 4096, a_mn, 0, seed=6, c_trans=True, pair=True, wide=wide)
+    _run(136, 520, 64, 1, 0, reduce_add=True, seed=7, c_trans=True, pair=True, wide=wide)
 
 
 def test_pair_tiles_reject_n_major_b(cuda_dev):
@@ -96,6 +100,7 @@ def test_pair_tiles_reject_n_major_b(cuda_dev):
     A = torch.zeros(64, 64, dtype=torch.bfloat16, device=dev)
     C = torch.zeros(64, 64, device=dev)
     ws = workspace(256, dev)
-    rc = _native.lib().kd_test_gemm(A.data_ptr(), A.data_ptr(), C.data_ptr(), 64, 64, 64, 0, 1, 4, ws.data_ptr(),
-                                    torch.cuda.current_stream().cuda_stream)
-    assert rc == 2  # KD_ERR_UNSUPPORTED, nothing launched
+    for flags in (4, 12):
+        rc = _native.lib().kd_test_gemm(A.data_ptr(), A.data_ptr(), C.data_ptr(), 64, 64, 64, 0, 1, flags,
+                                        ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert rc == 2  # KD_ERR_UNSUPPORTED, nothing launched

@@ -72,6 +72,16 @@ int gemm_cta2() {
   return kDefaultCta2;
 }
 
+// Width of the CTA-pair tiles per GEMM: wide (256 x 512) where the epilogue
+// is light (forward statistics, dH/dW), narrow (256 x 256, double-buffered
+// accumulators) for the dz and logit-storing epilogues. KD_GEMM_WIDE=0/1
+// forces one width everywhere (tests and measurements).
+int gemm_wide(int dflt) {
+  const char* e = std::getenv("KD_GEMM_WIDE");
+  if (e && (e[0] == '0' || e[0] == '1')) return e[0] - '0';
+  return dflt;
+}
+
 // The backward pass groups chunks for its dH/dW GEMM when chunks are small:
 // the fp32 dW read-modify-write (8 V d bytes) then happens once per group
 // instead of once per chunk. The workspace holds the group's dz.
@@ -276,13 +286,13 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
     return KD_ERR_UNSUPPORTED;
   Problem& P0 = ag.pr[0];
   P0.m_blocks = (int)ceil_div(d, TR);
-  P0.n_blocks = (int)ceil_div(grows, kBNGrad);
+  P0.n_blocks = (int)ceil_div(grows, gemm_tile_cols(ag.cta2, ag.wide));
   P0.k_blocks = (int)ceil_div(V, kBK);
   P0.a_mn = 1; P0.b_mn = 0; P0.M = (int)d; P0.N = grows;
   P0.tile_begin = 0; P0.n_fastest = 0; P0.reduce_add = 0; P0.c_trans = 1; P0.out_bf16 = dH_bf16;
   Problem& P1 = ag.pr[1];
   P1.m_blocks = (int)ceil_div(V, TR);
-  P1.n_blocks = (int)ceil_div(d, kBNGrad);
+  P1.n_blocks = (int)ceil_div(d, gemm_tile_cols(ag.cta2, ag.wide));
   P1.k_blocks = (int)ceil_div(grows, kBK);
   P1.a_mn = 1; P1.b_mn = 0; P1.M = (int)V; P1.N = (int)d;
   P1.tile_begin = P0.m_blocks * P0.n_blocks; P1.n_fastest = 1;
@@ -302,6 +312,7 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
 int grad_setup(GemmArgs& ag, const void* W, float* dW, int64_t d, int64_t V, int* status, int* counter) {
   std::memset(&ag, 0, sizeof(ag));
   ag.cta2 = gemm_cta2();
+  ag.wide = gemm_wide(1);
   ag.status = status;
   ag.tile_counter = counter;
   if (encode_map_2d(&ag.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, 64,
@@ -423,6 +434,7 @@ int kd_fused_kl_fwd_ex(const void* H, const void* W, const int32_t* ids, const f
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.cta2 = gemm_cta2();
+  a.wide = gemm_wide(1);
   a.zscale = o.inv_tau;
   const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
   if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
@@ -445,7 +457,7 @@ int kd_fused_kl_fwd_ex(const void* H, const void* W, const int32_t* ids, const f
       return KD_ERR_UNSUPPORTED;
     Problem& P = a.pr[0];
     P.m_blocks = (int)ceil_div(rows, TR);
-    P.n_blocks = (int)ceil_div(V, kBNLogits);
+    P.n_blocks = (int)ceil_div(V, gemm_tile_cols(a.cta2, a.wide));
     P.k_blocks = (int)ceil_div(d, kBK);
     P.a_mn = 0; P.b_mn = 0;
     P.M = rows; P.N = (int)V;
@@ -515,6 +527,7 @@ int kd_fused_kl_bwd_ex(const void* H, const void* W, const int32_t* ids, const f
   GemmArgs az, ag;
   std::memset(&az, 0, sizeof(az));
   az.cta2 = gemm_cta2();
+  az.wide = gemm_wide(0);
   az.zscale = o.inv_tau;
   const int TR = gemm_tile_rows(az.cta2), BR = gemm_b_box_rows(az.cta2);
   // W: K-major B of the logits GEMM, M-major A of the dH^T GEMM.
@@ -544,7 +557,7 @@ int kd_fused_kl_bwd_ex(const void* H, const void* W, const int32_t* ids, const f
     {
       Problem& P = az.pr[0];
       P.m_blocks = (int)ceil_div(grows, TR);
-      P.n_blocks = (int)ceil_div(V, kBNLogits);
+      P.n_blocks = (int)ceil_div(V, gemm_tile_cols(az.cta2, az.wide));
       P.k_blocks = (int)ceil_div(d, kBK);
       P.a_mn = 0; P.b_mn = 0; P.M = grows; P.N = (int)V;
       P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
@@ -618,6 +631,7 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
   GemmArgs a, ag;
   std::memset(&a, 0, sizeof(a));
   a.cta2 = gemm_cta2();
+  a.wide = gemm_wide(0);
   a.zscale = o.inv_tau;
   const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
   if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
@@ -645,7 +659,7 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
       return KD_ERR_UNSUPPORTED;
     Problem& P = a.pr[0];
     P.m_blocks = (int)ceil_div(grows, TR);
-    P.n_blocks = (int)ceil_div(V, kBNLogits);
+    P.n_blocks = (int)ceil_div(V, gemm_tile_cols(a.cta2, a.wide));
     P.k_blocks = (int)ceil_div(d, kBK);
     P.a_mn = 0; P.b_mn = 0; P.M = grows; P.N = (int)V;
     P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
@@ -718,6 +732,7 @@ int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_t d, in
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.cta2 = gemm_cta2();
+  a.wide = gemm_wide(0);
   a.zscale = 1.f;
   const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
   if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
@@ -732,7 +747,7 @@ int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_t d, in
       return KD_ERR_UNSUPPORTED;
     Problem& P = a.pr[0];
     P.m_blocks = (int)ceil_div(rows, TR);
-    P.n_blocks = (int)L.S;
+    P.n_blocks = (int)ceil_div(V, gemm_tile_cols(a.cta2, a.wide));
     P.k_blocks = (int)ceil_div(d, kBK);
     P.a_mn = 0; P.b_mn = 0; P.M = rows; P.N = (int)V;
     P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
@@ -776,7 +791,7 @@ int kd_test_wait_timeout(int64_t limit_ns, void* ws, void* stream) {
 int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int32_t a_mn,
                  int32_t b_mn, int32_t flags, void* ws, void* stream) {
   if (!A || !B || !C || !ws || M <= 0 || N <= 0 || K <= 0) return KD_ERR_INVALID_ARG;
-  const int reduce_add = flags & 1, c_trans = (flags >> 1) & 1, cta2 = (flags >> 2) & 1;
+  const int reduce_add = flags & 1, c_trans = (flags >> 1) & 1, cta2 = (flags >> 2) & 1, wide = (flags >> 3) & 1;
   const int64_t ldc = c_trans ? M : N;  // C is [M, N], or [N, M] when stored transposed
   if (K % 8 || (a_mn && M % 8) || (b_mn && N % 8) || ldc % 4) return KD_ERR_UNSUPPORTED;
   if (cta2 && b_mn) return KD_ERR_UNSUPPORTED;  // the pair tiles read a K-major B only
@@ -794,10 +809,11 @@ int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, i
                            : encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, 32);
   if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return KD_ERR_UNSUPPORTED;
   a.cta2 = cta2;
+  a.wide = wide;
   a.zscale = 1.f;
   Problem& P = a.pr[0];
   P.m_blocks = (int)ceil_div(M, gemm_tile_rows(cta2));
-  P.n_blocks = (int)ceil_div(N, kBNGrad);
+  P.n_blocks = (int)ceil_div(N, gemm_tile_cols(cta2, wide));
   P.k_blocks = (int)ceil_div(K, kBK);
   P.a_mn = a_mn ? 1 : 0; P.b_mn = b_mn ? 1 : 0;
   P.M = (int)M; P.N = (int)N;

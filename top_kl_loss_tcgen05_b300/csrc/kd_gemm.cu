@@ -37,13 +37,24 @@
 //               can hold a top-K element.
 // Two tile shapes:
 //   C2 = false  one CTA per 128 x 256 tile (tcgen05 cta_group::1, M = 128).
-//   C2 = true   a cluster of two CTAs per 256 x 256 tile (cta_group::2,
-//               M = 256). Each CTA loads its 128 rows of A and its 128-row
-//               half of B; the even CTA issues the MMAs, which read both
-//               CTAs' shared memory and write both CTAs' TMEM (each CTA
-//               holds its own 128 rows of the accumulator). Per SM this
-//               halves the B bytes loaded per MMA and leaves room for a
-//               deeper ring. B must be K-major.
+//   C2 = true   a cluster of two CTAs per tile (cta_group::2, M = 256);
+//               the even CTA issues the MMAs, which read both CTAs' shared
+//               memory and write both CTAs' TMEM (each CTA holds its own 128
+//               rows of the accumulator). B must be K-major. Two widths:
+//     WIDE = false  256 x 256: each CTA loads 128 rows of A and a 128-row
+//               half of B per K step; two 256-column accumulators let the
+//               epilogue of one tile overlap the MMAs of the next.
+//     WIDE = true   256 x 512: two N = 256 instructions per K step, each CTA
+//               loads 256 rows of B (two 128-row boxes). Per SM that moves
+//               48 bytes of operands per 1024 MMA cycles instead of 64, and
+//               operand supply is what limits the narrow tile on B300
+//               (8192^3: 1643 vs 1480 TF/s). The 512-column accumulator
+//               fills TMEM, so the epilogue runs between tiles; eight
+//               epilogue warps (two per TMEM lane quadrant, one per
+//               256-column half) keep that short. The wide tile pays off
+//               where the epilogue is light (the forward statistics, the
+//               dH/dW stores); the dz and the logit-storing epilogues stay
+//               narrow.
 // The logits tile therefore never leaves the chip in the forward pass. In
 // backward, only the chunk's dz (bf16, c x V) goes to HBM.
 #include <cstdint>
@@ -56,23 +67,27 @@ namespace kd {
 namespace {
 
 constexpr int EPI_FWD = 0, EPI_DZ = 1, EPI_GRAD = 2, EPI_FWDST = 3, EPI_TEACHER = 4;
-constexpr int kThreads = 192;  // 6 warps
-constexpr int BN = kBNLogits;  // N tile (all kernels)
+constexpr int BN = kBNLogits;  // columns one epilogue warp covers per tile (a vocabulary tile)
 static_assert(kBNLogits == kBNGrad, "one N tile for all GEMMs");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kStageBytesStaging = 4096;  // one 32-row x 128-byte staging buffer
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 
 
-template <int NS, int EPI, bool C2>
+template <int NS, int EPI, bool C2, bool WIDE>
 struct Cfg {
+  static constexpr bool W = C2 && WIDE;               // 256 x 512 pair tiles
   static constexpr int TM = C2 ? 2 * kBM : kBM;       // rows of a tile
-  static constexpr int BNL = C2 ? BN / 2 : BN;        // B rows held by one CTA
+  static constexpr int TN = W ? 2 * BN : BN;          // columns of a tile
+  static constexpr int NACC = W ? 1 : 2;              // TMEM accumulators (512 columns in all)
+  static constexpr int EPI_WARPS = W ? 8 : 4;         // two per TMEM lane quadrant when wide
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer + MMA + epilogue warps
+  static constexpr int BNL = (C2 && !WIDE) ? 128 : 256;  // B rows held by one CTA per K step
   static constexpr uint32_t A_BYTES = kBM * kBK * 2;  // this CTA's A block
   static constexpr uint32_t B_BYTES = BNL * kBK * 2;  // this CTA's B block
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
   static constexpr uint32_t TX = C2 ? 2 * STAGE : STAGE;  // bytes that complete one full-barrier phase
-  static constexpr uint32_t STG = (EPI == EPI_FWD) ? 0u : 4u * 2u * kStageBytesStaging;
+  static constexpr uint32_t STG = (EPI == EPI_FWD) ? 0u : (uint32_t)EPI_WARPS * 2u * kStageBytesStaging;
   static constexpr uint32_t BAR_OFF = NS * STAGE + STG;
   static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
   static_assert((2 * NS + 13) * 8 + 24 <= 256, "barrier block");
@@ -188,9 +203,10 @@ __device__ __forceinline__ void commit_x(uint64_t* bar) {
   }
 }
 
-template <int NS, int EPI, bool C2>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs g) {
-  using C = Cfg<NS, EPI, C2>;
+template <int NS, int EPI, bool C2, bool WIDE>
+__global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
+    gemm_kernel(const __grid_constant__ GemmArgs g) {
+  using C = Cfg<NS, EPI, C2, WIDE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -208,13 +224,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = C2 ? cluster_rank() : 0u;
   const bool leader = rank == 0;
-  // Readers that release a queue slot: the MMA thread and 4 epilogue warps,
-  // plus (C2) the odd CTA's producer and 4 epilogue warps.
-  constexpr uint32_t kQueueReaders = C2 ? 10u : 5u;
+  // Readers that release a queue slot: the MMA thread and the epilogue
+  // warps, plus (C2) the odd CTA's producer and epilogue warps.
+  constexpr uint32_t kQueueReaders = C2 ? 2u * (1u + C::EPI_WARPS) : 1u + C::EPI_WARPS;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], C2 ? 8 : 4); }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], (C2 ? 2 : 1) * C::EPI_WARPS);
+    }
     mbar_init(drain, 1);
     for (int q = 0; q < 4; ++q) { mbar_init(&tqf[q], 1); mbar_init(&tqe[q], kQueueReaders); }
     *abort_flag = 0;
@@ -271,7 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const CUtensorMap* mA = &g.tmA[tl.prob];
         const CUtensorMap* mB = &g.tmB[tl.prob];
         const int am = tl.mb * C::TM + (int)rank * kBM;  // this CTA's first A row (M)
-        const int bn = tl.nb * BN + (int)rank * C::BNL;  // this CTA's first B row (N)
+        // this CTA's first B row (N); wide pair tiles load a second box 256
+        // rows further
+        const int bn = C2 ? tl.nb * C::TN + (int)rank * 128 : tl.nb * C::TN;
         for (int kb = 0; kb < P.k_blocks; ++kb) {
           if (!mbar_wait<C2>(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t sA = smem_u32(smem + stage * C::STAGE);
@@ -285,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
               for (int q = 0; q < kBM / 64; ++q) tma_load_2d_pair(sA + q * 8192, mA, fb, am + q * 64, kb * kBK);
             }
-            tma_load_2d_pair(sB, mB, fb, kb * kBK, bn);
+            tma_load_2d_pair(sB, mB, fb, kb * kBK, bn);  // (wide: N half 0)
+            if (C::W) tma_load_2d_pair(sB + 16384, mB, fb, kb * kBK, bn + 256);  // N half 1
           } else {
             mbar_arrive_expect_tx(&full[stage], C::TX);
             if (!P.a_mn) {
@@ -346,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const Problem& P = g.pr[tl.prob];
         if (!mbar_wait<C2>(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);  // wide: acc = 0, columns [0, 512)
         const int b_mn = C2 ? 0 : P.b_mn;
         const uint32_t idesc = idesc_bf16_f32(C::TM, BN, P.a_mn, b_mn);
         for (int kb = 0; kb < P.k_blocks; ++kb) {
@@ -359,13 +381,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const uint64_t ad = P.a_mn ? sdesc_sw128(sA + k * 2048, 8192, 1024) : sdesc_sw128(sA + k * 32, 16, 1024);
             const uint64_t bd = b_mn ? sdesc_sw128(sB + k * 2048, 8192, 1024) : sdesc_sw128(sB + k * 32, 16, 1024);
             mma_x<C2>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            if (C::W)  // N half 1: B rows 256 further in smem, TMEM columns 256 further
+              mma_x<C2>(d_tmem + 256, ad, sdesc_sw128(sB + 16384 + k * 32, 16, 1024), idesc, (kb | k) != 0 ? 1u : 0u);
           }
           commit_x<C2>(&empty[stage]);
           if (++stage == NS) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         commit_x<C2>(&tfull[acc]);
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
       }
       if (!ok) {
         set_status(g.status, ST_TIMEOUT);
@@ -384,12 +408,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int wq = warp & 3;  // TMEM lane quadrant this warp may access
+    const int wq = warp & 3;        // TMEM lane quadrant this warp may access
+    const int ew = warp - 2;        // epilogue warp index
+    const int hc = C::W ? ew >> 2 : 0;  // wide: the 256-column half of the tile this warp covers
     int acc = 0;
     uint32_t acc_phase = 0;
     int buf = 0, nstore = 0;
     bool ok = true;
-    uint8_t* stg = smem + NS * C::STAGE + (uint32_t)wq * 2u * kStageBytesStaging;
+    uint8_t* stg = smem + NS * C::STAGE + (uint32_t)ew * 2u * kStageBytesStaging;
     for (int j = 0;; ++j) {
       const int qs = j & 3;
       if (!mbar_wait<C2>(&tqf[qs], (uint32_t)(j >> 2) & 1u, abort_flag)) ok = false;
@@ -406,7 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const Problem& P = g.pr[tl.prob];
       const int m0 = tl.mb * C::TM + (int)rank * kBM;  // first tile row held in this CTA's TMEM
       const int row = m0 + 32 * wq + lane;
-      const int n0 = tl.nb * BN;
+      const int vt = tl.nb * (C::TN / BN) + hc;  // the 256-column block (vocabulary tile) of this warp
+      const int n0 = vt * BN;
 
       // Teacher-id cursor of this row for the tile's vocabulary slice.
       int cnt = 0, k = 0;
@@ -425,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(acc * BN);
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)((acc + hc) * BN);
       // The loss epilogues work on z / tau: exp arguments use zl2 = log2(e) / tau
       // and the values they keep (tile maxima, logits at teacher ids) are
       // scaled by zscale = 1 / tau. With tau = 1 this is the plain logit.
@@ -466,9 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           ++nstore;
           buf ^= 1;
         }
-        if (row < g.rows) {
-          g.part_m[(size_t)row * g.S + tl.nb] = m;
-          g.part_s[(size_t)row * g.S + tl.nb] = s;
+        if (row < g.rows && n0 < g.V) {
+          g.part_m[(size_t)row * g.S + vt] = m;
+          g.part_s[(size_t)row * g.S + vt] = s;
         }
       } else if (EPI == EPI_FWDST) {
         // Pass 1: the row's maximum over the tile's valid columns.
@@ -540,9 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
           u = __reduce_min_sync(0xffffffffu, want);
         }
-        if (row < g.rows) {
-          g.part_m[(size_t)row * g.S + tl.nb] = m * zscale;
-          g.part_s[(size_t)row * g.S + tl.nb] = s;
+        if (row < g.rows && n0 < g.V) {
+          g.part_m[(size_t)row * g.S + vt] = m * zscale;
+          g.part_s[(size_t)row * g.S + vt] = s;
         }
       } else if (EPI == EPI_FWD) {
         float m = -INFINITY, s = 0.f;
@@ -587,9 +614,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
           u = __reduce_min_sync(0xffffffffu, want);
         }
-        if (row < g.rows) {
-          g.part_m[(size_t)row * g.S + tl.nb] = m * zscale;
-          g.part_s[(size_t)row * g.S + tl.nb] = s;
+        if (row < g.rows && n0 < g.V) {
+          g.part_m[(size_t)row * g.S + vt] = m * zscale;
+          g.part_s[(size_t)row * g.S + vt] = s;
         }
       } else if (EPI == EPI_DZ) {
         const float lse_r = (row < g.rows) ? __ldg(g.lse + row) : 0.f;
@@ -738,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (leader) mbar_arrive(&tempty[acc]);
         else mbar_arrive_remote(&tempty[acc], 0);
       }
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
     }
     if (!ok) {
       if (lane == 0) { set_status(g.status, ST_TIMEOUT); *abort_flag = 1; }
@@ -760,14 +787,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 // Clusters of the pair kernel that fit on the device at once (cached per
 // device and instantiation).
 template <typename KernelT>
-int max_pair_clusters(KernelT k, uint32_t smem) {
+int max_pair_clusters(KernelT k, int threads, uint32_t smem) {
   static int cache[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (cache[dev] > 0) return cache[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -785,16 +812,16 @@ int max_pair_clusters(KernelT k, uint32_t smem) {
   return n;
 }
 
-template <int NS, int EPI, bool C2>
+template <int NS, int EPI, bool C2, bool WIDE = false>
 cudaError_t launch(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  using C = Cfg<NS, EPI, C2>;
+  using C = Cfg<NS, EPI, C2, WIDE>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
-  auto k = gemm_kernel<NS, EPI, C2>;
+  auto k = gemm_kernel<NS, EPI, C2, WIDE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   int units = num_sms;  // CTAs, or CTA pairs, resident at once
   if (C2) {
-    units = max_pair_clusters(k, C::SMEM);
+    units = max_pair_clusters(k, C::THREADS, C::SMEM);
     if (units <= 0) units = num_sms / 2;
   }
   if (a.total_tiles < units) units = a.total_tiles;
@@ -802,12 +829,12 @@ cudaError_t launch(const GemmArgs& a, int num_sms, cudaStream_t s) {
   e = cudaMemsetAsync(a.tile_counter, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
   if (!C2) {
-    k<<<units, kThreads, C::SMEM, s>>>(a);
+    k<<<units, C::THREADS, C::SMEM, s>>>(a);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(units * 2), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -822,25 +849,24 @@ cudaError_t launch(const GemmArgs& a, int num_sms, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_logits_fwd(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  if (a.cta2) return launch<7, EPI_FWD, true>(a, num_sms, s);
-  return launch<4, EPI_FWD, false>(a, num_sms, s);
-}
-cudaError_t launch_logits_dz(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  if (a.cta2) return launch<6, EPI_DZ, true>(a, num_sms, s);
-  return launch<4, EPI_DZ, false>(a, num_sms, s);
-}
+// Stages per width: narrow pair tiles 6 x 32 KB (7 without epilogue
+// staging), wide pair tiles 3 x 48 KB with 64 KB of staging for eight
+// epilogue warps (4 without), one CTA per tile 4 x 48 KB.
+#define KD_GEMM_DISPATCH(EPI, NS_NARROW, NS_WIDE)                 \
+  if (a.cta2 && a.wide) return launch<NS_WIDE, EPI, true, true>(a, num_sms, s); \
+  if (a.cta2) return launch<NS_NARROW, EPI, true, false>(a, num_sms, s);        \
+  return launch<4, EPI, false, false>(a, num_sms, s);
+
+cudaError_t launch_logits_fwd(const GemmArgs& a, int num_sms, cudaStream_t s) { KD_GEMM_DISPATCH(EPI_FWD, 7, 4) }
+cudaError_t launch_logits_dz(const GemmArgs& a, int num_sms, cudaStream_t s) { KD_GEMM_DISPATCH(EPI_DZ, 6, 3) }
 cudaError_t launch_logits_fwd_store(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  if (a.cta2) return launch<6, EPI_FWDST, true>(a, num_sms, s);
-  return launch<4, EPI_FWDST, false>(a, num_sms, s);
+  KD_GEMM_DISPATCH(EPI_FWDST, 6, 3)
 }
 cudaError_t launch_logits_teacher(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  if (a.cta2) return launch<6, EPI_TEACHER, true>(a, num_sms, s);
-  return launch<4, EPI_TEACHER, false>(a, num_sms, s);
+  KD_GEMM_DISPATCH(EPI_TEACHER, 6, 3)
 }
-cudaError_t launch_grad(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  if (a.cta2) return launch<6, EPI_GRAD, true>(a, num_sms, s);
-  return launch<4, EPI_GRAD, false>(a, num_sms, s);
-}
+cudaError_t launch_grad(const GemmArgs& a, int num_sms, cudaStream_t s) { KD_GEMM_DISPATCH(EPI_GRAD, 6, 3) }
+
+#undef KD_GEMM_DISPATCH
 
 }  // namespace kd

@@ -56,12 +56,17 @@ struct GemmArgs {
   const uint8_t* mask;    // [rows] chunk slice of the position mask (0 = excluded), or null
   int* status;            // device status word
   int cta2;               // 1: cluster-pair tiles (256 rows, tcgen05 cta_group::2)
+  int wide;               // with cta2: 1 = 256 x 512 tiles, 0 = 256 x 256
 };
 
 // Rows of one GEMM tile (M extent) for the chosen tile shape; with cta2 the B
-// operand's tensor map box is 128 rows (each CTA of the pair loads half).
+// operand's tensor map box is 128 rows (each CTA of the pair loads one such
+// box per K step, two for wide tiles: one per 256-column half).
 inline int gemm_tile_rows(int cta2) { return cta2 ? 2 * kBM : kBM; }
 inline int gemm_b_box_rows(int cta2) { return cta2 ? kBNLogits / 2 : kBNLogits; }
+// Columns of one GEMM tile (N extent): 512 for wide CTA-pair tiles, 256
+// otherwise. Per-vocabulary-tile partials stay per 256 columns either way.
+inline int gemm_tile_cols(int cta2, int wide) { return (cta2 && wide) ? 2 * kBNLogits : kBNLogits; }
 
 cudaError_t encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                           uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
