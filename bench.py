@@ -220,6 +220,9 @@ def cpu_baseline(wl, budget_s: float = 15.0):
     cw = cpu_workload(wl)
     rows = size_sample(cw, budget_s)
     t = oracle_sample(cw, rows)
+    if t < 0.4 * budget_s and rows < len(cw["ids"]):  # the fit underestimated the per-row cost
+        rows = int(min(len(cw["ids"]), rows * min(4.0, budget_s / max(t, 1e-3))))
+        t = oracle_sample(cw, rows)
     return {"value": rows / t, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
             "sample": "fp64 numpy oracle, forward + backward (loss, lse, dH, dW contribution) of the first %d "
                       "positions of the workload at full d and V; %.1f s" % (rows, t)}
