@@ -14,8 +14,9 @@ extern "C" {
 #endif
 
 /* C = A * B^T (fp32, row-major, device) on the tcgen05 GEMM that the
- * backward pass uses for dH and dW (128 x 256 tiles, dynamic tile
- * scheduling, TMA loads, TMEM accumulators, TMA store / reduce-add).
+ * backward pass uses for dH and dW (dynamic tile scheduling, TMA loads, TMEM
+ * accumulators, TMA store / reduce-add). The tile shape follows `flags`:
+ * one CTA per 128 x 256 tile by default.
  *   A: a_mn == 0 -> [M, K] row-major; a_mn == 1 -> [K, M] row-major (bf16).
  *   B: b_mn == 0 -> [N, K] row-major; b_mn == 1 -> [K, N] row-major (bf16).
  *   flags bit 0: add into C instead of overwriting it.

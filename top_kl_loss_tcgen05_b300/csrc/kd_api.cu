@@ -63,8 +63,9 @@ int num_sms_current() {
   return n;
 }
 
-// GEMM tile shape: 1 = CTA-pair tiles (256 x 256, tcgen05 cta_group::2),
-// 0 = one CTA per 128 x 256 tile. KD_GEMM_CTA2=0/1 overrides the default.
+// GEMM tile shape: 1 = CTA-pair tiles (tcgen05 cta_group::2; 256 x 512 or
+// 256 x 256, see gemm_wide), 0 = one CTA per 128 x 256 tile. KD_GEMM_CTA2=0/1
+// overrides the default.
 constexpr int kDefaultCta2 = 1;
 int gemm_cta2() {
   const char* e = std::getenv("KD_GEMM_CTA2");
@@ -464,7 +465,7 @@ int kd_fused_kl_fwd_ex(const void* H, const void* W, const int32_t* ids, const f
     P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0;
     a.nprob = 1;
     a.total_tiles = P.m_blocks * P.n_blocks;
-    a.rows = rows; a.row_stride = (int)gchunk; a.S = (int)L.S; a.V = (int)V; a.Kp = L.Kp;
+    a.rows = rows; a.S = (int)L.S; a.V = (int)V; a.Kp = L.Kp;
     a.ids_sorted = ids_sorted; a.p_sorted = p_sorted; a.cnt = cnt;
     a.zK = zK; a.part_m = part_m; a.part_s = part_s;
     a.status = status;
@@ -563,7 +564,7 @@ int kd_fused_kl_bwd_ex(const void* H, const void* W, const int32_t* ids, const f
       P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
       az.nprob = 1;
       az.total_tiles = P.m_blocks * P.n_blocks;
-      az.rows = grows; az.row_stride = (int)gchunk; az.V = (int)V; az.Kp = L.Kp;
+      az.rows = grows; az.V = (int)V; az.Kp = L.Kp;
       az.ids_sorted = ids_sorted; az.p_sorted = p_sorted; az.cnt = cnt;
       az.lse = lse + g0; az.scale = 1.f; az.dscale = wscale;
       az.mask = mask_at(o, g0);
@@ -665,7 +666,7 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
     P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
     a.nprob = 1;
     a.total_tiles = P.m_blocks * P.n_blocks;
-    a.rows = grows; a.row_stride = (int)gchunk; a.S = (int)L.S; a.V = (int)V; a.Kp = L.Kp;
+    a.rows = grows; a.S = (int)L.S; a.V = (int)V; a.Kp = L.Kp;
     a.ids_sorted = ids_sorted; a.p_sorted = p_sorted; a.cnt = cnt;
     a.zK = zK; a.part_m = part_m; a.part_s = part_s;
     a.status = status;
@@ -753,7 +754,7 @@ int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_t d, in
     P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
     a.nprob = 1;
     a.total_tiles = P.m_blocks * P.n_blocks;
-    a.rows = rows; a.row_stride = (int)chunk; a.S = (int)L.S; a.V = (int)V;
+    a.rows = rows; a.S = (int)L.S; a.V = (int)V;
     a.part_m = part_m; a.part_s = part_s;
     a.status = words;
     a.tile_counter = reinterpret_cast<int*>(w + kCounterOffset);

@@ -39,7 +39,6 @@ struct GemmArgs {
   int* tile_counter;      // dynamic tile scheduler (zeroed before each launch)
   // fused-epilogue data (chunk-local rows)
   int rows;               // rows of this chunk
-  int row_stride;         // chunk (rows of the per-chunk arrays)
   int S;                  // vocabulary tiles: row stride of the [chunk][S] partials
   int V;
   int Kp;                 // row stride of the sorted id / p / zK arrays
