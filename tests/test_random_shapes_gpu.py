@@ -1,0 +1,61 @@
+"""Seeded random shapes through the fused loss (forward, backward and the
+single call) against the fp64 oracle, cycling through the GEMM tile
+configurations: one CTA per tile, CTA pairs at the default widths, all
+narrow, all wide. The shapes are ragged in every dimension (T, d, V, K,
+chunk), with small and tile-edge values."""
+
+import numpy as np
+import pytest
+import torch
+
+import top_kl_loss_tcgen05_b300 as kd
+from oracle import kd_oracle as O
+from top_kl_loss_tcgen05_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+MODES = [("0", None), ("1", None), ("1", "0"), ("1", "1")]
+
+
+def _shapes(n=24, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        T = int(rng.choice([1, 2, int(rng.integers(3, 700))]))
+        d = int(8 * rng.integers(1, 48))
+        V = int(rng.choice([int(rng.integers(1, 300)), int(rng.integers(300, 5000)), 256, 512, 513]))
+        K = int(min(V, rng.integers(1, 150)))
+        chunk = int(rng.choice([1, int(rng.integers(2, 300)), 1024]))
+        out.append((T, d, V, K, chunk, MODES[i % len(MODES)], 5000 + i))
+    return out
+
+
+def frob(a, b):
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(np.asarray(a, np.float64) - b) / nb) if nb > 0 else float(np.linalg.norm(a))
+
+
+@pytest.mark.parametrize("T,d,V,K,chunk,mode,seed", _shapes())
+def test_random_shape_matches_oracle(cuda_dev, monkeypatch, T, d, V, K, chunk, mode, seed):
+    monkeypatch.setenv("KD_GEMM_CTA2", mode[0])
+    if mode[1] is None:
+        monkeypatch.delenv("KD_GEMM_WIDE", raising=False)
+    else:
+        monkeypatch.setenv("KD_GEMM_WIDE", mode[1])
+    H, W = synth.student(T, d, V, seed)
+    ids, logp = synth.synthetic_cache(T, V, K, seed + 1)
+    H, W, ids, logp = H.to(cuda_dev), W.to(cuda_dev), ids.to(cuda_dev), logp.to(cuda_dev)
+    Hn, Wn = H.float().cpu().numpy(), W.float().cpu().numpy()
+    i, lp = ids.cpu().numpy(), logp.cpu().numpy()
+    lo, lse_o, L_o = O.fused_kl_forward(Hn, Wn, i, lp)
+    dH_o, dW_o = O.fused_kl_backward(Hn, Wn, i, lp, 1.0 / T)
+    loss, lse, rows = kd.fused_kl_fwd(H, W, ids, logp, chunk, want_rows=True)
+    dH, dW = kd.fused_kl_bwd(H, W, ids, logp, lse, chunk, 1.0 / T)
+    l1, lse1, r1, dH1, dW1 = kd.fused_kl_fwdbwd(H, W, ids, logp, chunk, want_rows=True)
+    torch.cuda.synchronize()
+    for lv, lsev, rv, dHv, dWv in ((loss, lse, rows, dH, dW), (l1, lse1, r1, dH1, dW1)):
+        assert abs(lv.item() - lo) <= 1e-3 * abs(lo) + 1e-6
+        np.testing.assert_allclose(lsev.cpu().numpy(), lse_o, rtol=1e-5, atol=1e-5)
+        np.testing.assert_allclose(rv.cpu().numpy(), L_o, rtol=1e-3, atol=2e-4)
+        assert frob(dHv.cpu().numpy(), dH_o) <= 1e-2
+        assert frob(dWv.cpu().numpy(), dW_o) <= 1e-2
