@@ -65,6 +65,18 @@ def kernel_src_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def gemm_tiles_desc() -> str:
+    """The GEMM tile shapes this process runs (KD_GEMM_CTA2 / KD_GEMM_WIDE
+    override the per-kernel defaults)."""
+    if os.environ.get("KD_GEMM_CTA2") == "0":
+        return "128x256 per CTA"
+    wide = os.environ.get("KD_GEMM_WIDE")
+    if wide in ("0", "1"):
+        return "%s per CTA pair (tcgen05 cta_group::2), every GEMM" % ("256x512" if wide == "1" else "256x256")
+    return ("256x512 per CTA pair for the logits forward and dH/dW GEMMs, 256x256 for dz, the single call's "
+            "forward and the teacher (tcgen05 cta_group::2)")
+
+
 def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources and this workload; else None."""
@@ -593,8 +605,7 @@ def main():
             "config": {"workload": describe(args.workload), "parallelism": "replicas" if world > 1 else "1 gpu",
                        "l2": "inputs larger than L2 (W alone is %.0f MB)" % (V * d * 2 / 1e6),
                        "teacher_cache": "kd_topk_cache of fp32 perturbed-W teacher logits",
-                       "gemm_tiles": "128x256 per CTA" if os.environ.get("KD_GEMM_CTA2") == "0"
-                       else "256x256 per CTA pair (tcgen05 cta_group::2)"},
+                       "gemm_tiles": gemm_tiles_desc()},
             "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
             "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "topk_extraction": topk, "fused_fwdbwd": fwdbwd,
             "teacher_topk": teacher,

@@ -167,8 +167,11 @@ KD_API int kd_topk_cache_noalloc(const void* logits, int32_t dtype, int64_t T, i
  *         be distinct within a row. Duplicates are summed, as the scatter-add
  *         gradient does. An id outside [0, V) is ignored and sets
  *         KD_ERR_BAD_ID in the status word.
- *   chunk positions per chunk, 1 <= chunk. The workspace grows as chunk * V;
- *         the chunk size changes results only by fp32 rounding order.
+ *   chunk positions per chunk, 1 <= chunk. The chunk size changes results
+ *         only by fp32 rounding order. The backward runs its dH/dW GEMM over
+ *         groups of G = clamp(4096 / chunk, 1, 4) chunks (integer division),
+ *         and the workspace holds one group's bf16 dz: about
+ *         2 * G * chunk * V bytes, at most 8 * chunk * V.
  *   Requires d % 8 == 0 (16-byte rows for TMA), 16-byte aligned H and W,
  *   1 <= K <= 4096, 1 <= V < 2^31.
  *   Workspace: kd_fused_kl_workspace_size(d, V, K, chunk) bytes. It does not

@@ -58,14 +58,17 @@ def test_status_strings(lib):
     assert lib.kd_version() >= 100
 
 
-def test_fused_workspace_is_independent_of_T_and_linear_in_chunk(lib):
+def test_fused_workspace_is_independent_of_T_and_follows_the_group_rule(lib):
     f = lib.kd_fused_kl_workspace_size
-    a = f(2880, 201088, 100, 2048)
-    b = f(2880, 201088, 100, 4096)
-    assert a > 0 and b > 0
-    # dominated by the bf16 dz chunk: chunk * V * 2 bytes
-    assert 2048 * 201088 * 2 < a < 1.05 * 2048 * 201088 * 2 + 64 * 2**20
-    assert 1.9 < b / a < 2.1
+    V = 201088
+    # dominated by the bf16 dz of one backward group of G = clamp(4096 / chunk, 1, 4)
+    # chunks: G * chunk * V * 2 bytes
+    for chunk, G in ((64, 4), (1024, 4), (1500, 2), (2048, 2), (3000, 1), (4096, 1), (8192, 1)):
+        n = f(2880, V, 100, chunk)
+        dz = G * chunk * V * 2
+        assert dz < n < 1.05 * dz + 64 * 2**20, (chunk, n, dz)
+        assert n <= 8 * chunk * V + 64 * 2**20
+    assert 1.9 < f(2880, V, 100, 128) / f(2880, V, 100, 64) < 2.1
     assert f(0, 10, 1, 1) == 0 and f(8, 0, 1, 1) == 0 and f(8, 10, 0, 1) == 0 and f(8, 10, 1, 0) == 0
 
 

@@ -52,7 +52,7 @@ def case(T, d, V, K, seed):
 
 @pytest.mark.parametrize("T,d,V,K,chunk", [
     (1, 8, 17, 1, 1),          # one position, K = 1, the smallest d
-    (5, 64, 300, 3, 1),        # chunk = 1: a group per position pair
+    (5, 64, 300, 3, 1),        # chunk = 1: groups of four positions, the last ragged
     (10, 128, 5000, 1, 4096),  # chunk > T, K = 1
     (64, 256, 8192, 4096, 64), # the largest supported K (block-wide teacher prep)
 ])

@@ -96,7 +96,7 @@ def test_matches_separate_calls_and_is_reproducible(cuda_dev):
 
 
 @pytest.mark.parametrize("T,d,V,K,chunk", [
-    (300, 264, 1000, 7, 128),     # ragged T, d, V; two groups, the last ragged
+    (1100, 264, 1000, 7, 128),    # ragged T, d, V; three groups of four chunks, the last ragged
     (129, 72, 4099, 33, 64),
     (64, 520, 257, 5, 64),        # V = one full vocabulary tile + 1
     (77, 8, 31, 3, 16),           # tiny d and V

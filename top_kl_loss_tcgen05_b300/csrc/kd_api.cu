@@ -83,10 +83,15 @@ int gemm_wide(int dflt) {
   return dflt;
 }
 
-// The backward pass groups chunks for its dH/dW GEMM when chunks are small:
-// the fp32 dW read-modify-write (8 V d bytes) then happens once per group
-// instead of once per chunk. The workspace holds the group's dz.
-int64_t bwd_group(int64_t chunk) { return chunk < 2048 ? 2 : 1; }
+// The backward pass groups chunks for its dH/dW GEMM, up to 4 chunks and
+// about 4096 positions per group. The dW tiles then run over a long
+// contraction (G * chunk), so their epilogue (the fp32 read-modify-write of
+// the tile, 8 V d bytes per group in all) is paid once per group, not once
+// per chunk. The workspace holds the group's dz: still O(chunk * V).
+int64_t bwd_group(int64_t chunk) {
+  const int64_t g = 4096 / chunk;
+  return g < 1 ? 1 : (g > 4 ? 4 : g);
+}
 
 // Fused-loss workspace layout (all offsets 256-byte aligned; dz 1024). One
 // layout serves the forward, the backward and the single-call forward +
