@@ -9,8 +9,10 @@ flops), so:
   * the scalar loss must equal the mean of the per-position losses, a
     property that holds at any size;
   * dW (a sum over all positions) is compared in full on a T-truncated run
-    with the same d, V and chunk: two chunks plus a ragged tail of 37
-    positions (one chunk plus the tail for the long-context workload).
+    with the same d, V and chunk: one full backward group (G chunks, with
+    G = clamp(4096 / chunk, 1, 4) as include/kd.h states) plus a ragged
+    second group of 37 positions, so that the second group's dW is added to
+    the first one's.
 The teacher cache is synthetic (K distinct ids per row), so that no oracle
 input comes from the CUDA path.
 """
@@ -81,7 +83,8 @@ def test_full_size_sampled_positions(cuda_dev, name):
 def test_full_width_dW_on_truncated_run(cuda_dev, name):
     c = synth.CONFIGS[name]
     chunk = c["chunk"]
-    Tp = (chunk + 37) if name == "long" else (2 * chunk + 37)
+    G = min(4, max(1, 4096 // chunk))  # chunks per backward group (include/kd.h)
+    Tp = G * chunk + 37
     c, H, W, ids, logp = _inputs(name, T=Tp)
     _, lse, _ = kd.fused_kl_fwd(H, W, ids, logp, chunk)
     dH, dW = kd.fused_kl_bwd(H, W, ids, logp, lse, chunk, 1.0 / Tp)

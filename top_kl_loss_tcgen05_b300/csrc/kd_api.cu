@@ -5,7 +5,7 @@
 // Knowledge Distillation มีประสิทธิภาพ..." (ai-thai.com), section "กลไก Fused
 // Chunked KL Loss"; "Multiverse Computing сократила видеопамять..."
 // (iitog.ru), fourth paragraph). Positions are processed one group of G
-// chunks at a time (G = 2 below 2048 positions per chunk, else 1):
+// chunks at a time (G = clamp(4096 / chunk, 1, 4), see bwd_group):
 //   forward : prep -> logits GEMM with (max, sum, gather) epilogue -> merge
 //   backward: prep -> logits GEMM recompute with dz epilogue -> dH + dW GEMMs
 //   fwdbwd  : prep -> logits GEMM storing exp(z - m_tile) -> merge -> dz pass
