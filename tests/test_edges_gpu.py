@@ -55,6 +55,8 @@ def case(T, d, V, K, seed):
     (5, 64, 300, 3, 1),        # chunk = 1: groups of four positions, the last ragged
     (10, 128, 5000, 1, 4096),  # chunk > T, K = 1
     (64, 256, 8192, 4096, 64), # the largest supported K (block-wide teacher prep)
+    (5000, 64, 700, 5, 1365),  # groups of three chunks (4095 positions), the second ragged
+    (5000, 64, 700, 5, 4097),  # chunk above 4096: groups of one chunk
 ])
 def test_loss_edges_match_oracle(cuda_dev, T, d, V, K, chunk):
     run_all(*case(T, d, V, K, T * 31 + K), chunk)
