@@ -84,8 +84,8 @@ def gemm_tiles_desc() -> str:
     wide = os.environ.get("KD_GEMM_WIDE")
     if wide in ("0", "1"):
         return "%s per CTA pair (tcgen05 cta_group::2), every GEMM" % ("256x512" if wide == "1" else "256x256")
-    return ("256x512 per CTA pair for the logits forward and dH/dW GEMMs, 256x256 for dz, the single call's "
-            "forward and the teacher (tcgen05 cta_group::2)")
+    return ("256x512 per CTA pair for every GEMM but the dz recompute, which uses 256x256 "
+            "(tcgen05 cta_group::2)")
 
 
 def ncu_traffic(kernel: str, workload: str):

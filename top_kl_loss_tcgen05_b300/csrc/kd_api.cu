@@ -73,10 +73,12 @@ int gemm_cta2() {
   return kDefaultCta2;
 }
 
-// Width of the CTA-pair tiles per GEMM: wide (256 x 512) where the epilogue
-// is light (forward statistics, dH/dW), narrow (256 x 256, double-buffered
-// accumulators) for the dz and logit-storing epilogues. KD_GEMM_WIDE=0/1
-// forces one width everywhere (tests and measurements).
+// Width of the CTA-pair tiles per GEMM, chosen by measurement on B300: wide
+// (256 x 512, one accumulator) for the forward statistics, dH/dW, the
+// single call's exp-storing forward and the teacher logits; narrow (256 x 256,
+// double-buffered accumulators, so the epilogue overlaps the next tile) for
+// the dz recompute, whose epilogue costs more than the wide tile saves.
+// KD_GEMM_WIDE=0/1 forces one width everywhere (tests and measurements).
 int gemm_wide(int dflt) {
   const char* e = std::getenv("KD_GEMM_WIDE");
   if (e && (e[0] == '0' || e[0] == '1')) return e[0] - '0';
@@ -637,7 +639,7 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
   GemmArgs a, ag;
   std::memset(&a, 0, sizeof(a));
   a.cta2 = gemm_cta2();
-  a.wide = gemm_wide(0);
+  a.wide = gemm_wide(1);
   a.zscale = o.inv_tau;
   const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
   if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
@@ -738,7 +740,7 @@ int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_t d, in
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.cta2 = gemm_cta2();
-  a.wide = gemm_wide(0);
+  a.wide = gemm_wide(1);
   a.zscale = 1.f;
   const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
   if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
