@@ -42,7 +42,10 @@
  *    elements) is given. bf16 is IEEE bfloat16 (1-8-7) stored as uint16.
  *  - `stream` is a cudaStream_t cast to void*. NULL means the legacy default
  *    stream. Calls enqueue their work and return without synchronising.
- *    Calls that share one workspace must not overlap on the GPU.
+ *    Calls that share one workspace must not overlap on the GPU. Calls on
+ *    distinct workspaces may run concurrently: on different streams, and
+ *    from different host threads (except kd_topk_cache_noalloc, whose
+ *    scratch is shared).
  *  - Argument errors come back synchronously, before anything is launched,
  *    as KD_ERR_INVALID_ARG / KD_ERR_UNSUPPORTED / KD_ERR_WORKSPACE. A failed
  *    launch returns KD_ERR_CUDA. Errors found on the device are recorded in a

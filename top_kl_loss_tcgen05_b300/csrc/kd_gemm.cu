@@ -57,6 +57,7 @@
 //               narrow.
 // The logits tile therefore never leaves the chip in the forward pass. In
 // backward, only the chunk's dz (bf16, c x V) goes to HBM.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -788,10 +789,13 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
 // device and instantiation).
 template <typename KernelT>
 int max_pair_clusters(KernelT k, int threads, uint32_t smem) {
-  static int cache[64] = {0};
+  // Atomic: launches on distinct workspaces may come from several host
+  // threads; every thread computes the same value, so the first store wins.
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev] > 0) return cache[dev];
+  const int cached = cache[dev].load(std::memory_order_relaxed);
+  if (cached > 0) return cached;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(threads, 1, 1);
@@ -808,7 +812,7 @@ int max_pair_clusters(KernelT k, int threads, uint32_t smem) {
     (void)cudaGetLastError();
     return 0;
   }
-  cache[dev] = n;
+  cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
