@@ -10,6 +10,7 @@ import torch
 import top_kl_loss_tcgen05_b300 as kd
 from oracle import kd_oracle as O
 from top_kl_loss_tcgen05_b300 import synth
+from topk_props import check_topk_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -88,7 +89,8 @@ def test_topk_large_K_exact_path(cuda_dev):
 def test_topk_full_size_workload_sampled(cuda_dev):
     """The extraction workload at its full size ([8192, 201088] bf16, N(0,2)
     plus a Zipf-like per-row bias). All rows run in one launch, as in the
-    bench; the oracle checks 256 rows spread over the matrix."""
+    bench. The oracle checks 256 rows spread over the matrix, and every row
+    passes the exact property check of tests/topk_props.py."""
     c = synth.CONFIGS["topk"]
     x = synth.topk_logits(c["T"], c["V"], c["seed"], device=cuda_dev)
     ws = kd.workspace(256, cuda_dev)
@@ -108,3 +110,4 @@ def test_topk_full_size_workload_sampled(cuda_dev):
     assert bool((srt[:, 1:] != srt[:, :-1]).all())
     fallback_rows = int(ws[4:8].view(torch.int32).item())
     assert fallback_rows < c["T"] // 20  # the radix path is the exception
+    check_topk_rows(x, ids, logp, LOGP_TOL)  # all 8192 rows
