@@ -631,7 +631,7 @@ def main():
     topk = None if args.no_topk else bench_topk(dev, peaks, rows=args.topk_rows)
     teacher = None if args.no_teacher else bench_teacher(dev, peaks)
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:  # a reported baseline at N=1 only
         cpu = cpu_baseline(wl)
 
     if rank == 0:
