@@ -64,15 +64,15 @@ def _code_only(src: str) -> str:
     return "\n".join(ln for ln in lines if ln)
 
 
-def kernel_src_hash() -> str:
-    """Identifies the CUDA sources (code, not comments) that the ncu traffic
-    record was taken on."""
+def kernel_src_hash(files=None) -> str:
+    """Identifies CUDA sources (code, not comments) that an ncu traffic record
+    was taken on: the listed files of the package's csrc/, else all of them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "top_kl_loss_tcgen05_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
-                h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
+    names = sorted(files) if files else sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for f in names:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -98,7 +98,7 @@ def ncu_traffic(kernel: str, workload: str):
     except Exception:
         return None
     e = d.get(kernel, {}).get(workload)
-    if not e or e.get("src_sha") != kernel_src_hash():
+    if not e or e.get("src_sha") != kernel_src_hash(e.get("src_files")):
         return None
     return e.get("dram_bytes_per_launch")
 
