@@ -54,6 +54,21 @@ def test_topk_heavy_ties_small_ints(cuda_dev, dtype):
         _check(xd, K, force_exact=True)
 
 
+@pytest.mark.parametrize("dtype,V", [(torch.float32, 20011), (torch.bfloat16, 40009)])
+def test_topk_rows_with_full_batches(cuda_dev, dtype, V):
+    """Rows long enough for full load batches (6 x 256 vectors of 16 bytes:
+    6144 fp32 or 12288 bf16 elements), the common case at real vocabulary
+    sizes, with a ragged tail; the whole result against the oracle. The
+    values are heavy-tailed and rounded to a coarse grid, so the top-K
+    boundary has ties."""
+    g = torch.Generator().manual_seed(V)
+    x = (torch.randn(24, V, generator=g) * 3).round() / 4
+    x[3] = 0.0  # one row all ties
+    x[5, ::7] = 9.0  # many equal maxima
+    _check(x.to(dtype).to(cuda_dev), 100)
+    _check(x.to(dtype).to(cuda_dev), 1)
+
+
 def test_topk_degenerate_rows(cuda_dev):
     V = 1000
     rows = [torch.zeros(V), torch.full((V,), -3.5), torch.arange(V, dtype=torch.float32),
