@@ -101,10 +101,12 @@ KD_API int kd_version(void);
  *           (the full-vocabulary log-softmax at those ids), computed in fp32.
  *   Requires 1 <= K <= V, V < 2^31, and finite logits. The logits pointer
  *   needs only element alignment, and any ld is accepted (each row is read
- *   with 16-byte loads from its first 16-byte boundary). Rows are selected from per-thread
- *   candidate lists (K <= 2048). A row where that could miss an element
- *   (heavy ties at the K-th value, or K > 2048) is redone by an exact radix
- *   selection. Both paths give the same result.
+ *   with 16-byte loads from its first 16-byte boundary). For K <= 1024 a row
+ *   is streamed once for its log-sum-exp and a lower bound of its K-th value,
+ *   and the elements at or above that bound (collected into a buffer of 2048)
+ *   are sorted. A row whose buffer overflows (heavy ties at the K-th value)
+ *   or K > 1024 is redone by an exact radix selection. Both paths give the
+ *   same result.
  *   Workspace: kd_topk_workspace_size(T, V, K, dtype) bytes: the status word,
  *   then (second int32) a running count of rows that took the radix path.
  */

@@ -98,7 +98,9 @@ def test_topk_unaligned_stride_and_ragged_V(cuda_dev):
 def test_topk_large_K_exact_path(cuda_dev):
     g = torch.Generator().manual_seed(4)
     x = torch.randn(6, 9000, generator=g).to(torch.bfloat16).to(cuda_dev)
-    _check(x, 2500)  # K > 2048 goes to the radix selection directly
+    _check(x, 1024)  # the largest K of the candidate-buffer path
+    _check(x, 1500)  # K > 1024 goes to the radix selection directly
+    _check(x, 2500)
 
 
 def test_topk_full_size_workload_sampled(cuda_dev):
