@@ -51,9 +51,9 @@
 //               (8192^3: 1643 vs 1480 TF/s). The 512-column accumulator
 //               fills TMEM, so the epilogue runs between tiles; eight
 //               epilogue warps (two per TMEM lane quadrant, one per
-//               256-column half) keep that short. The wide tile pays off
-//               where the epilogue is light (the forward statistics, the
-//               dH/dW stores); the dz and the logit-storing epilogues stay
+//               256-column half) keep that short. Measured per GEMM, the
+//               wide tile pays off everywhere but in the dz recompute, whose
+//               epilogue costs more than the wide tile saves; that one stays
 //               narrow.
 // The logits tile therefore never leaves the chip in the forward pass. In
 // backward, only the chunk's dz (bf16, c x V) goes to HBM.
