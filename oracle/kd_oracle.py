@@ -30,7 +30,7 @@ and section:
   alteraram?": KL divergence measures how far the student's predictions are
   from the teacher's.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * KL direction is KL(p_teacher || q_student). It is the only direction that
   stays finite when the teacher has no mass outside its K cached ids.

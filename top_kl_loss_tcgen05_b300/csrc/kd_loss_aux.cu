@@ -17,9 +17,9 @@
 //          from unrounded values exactly as in the recompute path.
 // All reductions run in a fixed order, so the loss is bitwise reproducible.
 // Definition: "ทำให้ Knowledge Distillation มีประสิทธิภาพ..." (ai-thai.com),
-// section "กลไก Fused Chunked KL Loss". The KL direction, the
-// renormalisation over K and the mean over positions are this build's
-// readings (the page states no formula).
+// section "กลไก Fused Chunked KL Loss". The page states no formula: the KL
+// direction (teacher to student), the renormalisation of the teacher over K
+// and the mean over positions are the readings its text supports.
 #include <cstdint>
 #include <cuda_runtime.h>
 

@@ -4,7 +4,7 @@ This module only draws random numbers and builds input tensors. It holds no
 step of the method: no softmax, no top-K selection and no KL. Both the CUDA
 path and the oracle take their inputs from here.
 
-Workloads (sizes from the pages' settings, see DESIGN.md "Input recipe"):
+Workloads (sizes from the pages' settings):
 
 * Student: H ~ N(0, 1) [T, d] and W ~ N(0, 1/d) [V, d], both bf16. The
   second argument of N is the variance, so each logit H W^T has unit variance.
