@@ -4,8 +4,9 @@ times (same T, d, V, K and chunk).
 The full fp64 oracle over all T positions is out of reach here (up to 1e15
 flops), so:
   * lse, the per-position loss L_t and dH_t are compared on a seeded sample
-    of positions. It includes the first and last positions and chunk
-    boundaries, and the oracle computes each sampled row on its own;
+    of positions, for the separate calls and for the single call. It
+    includes the first and last positions and chunk and group boundaries,
+    and the oracle computes each sampled row on its own;
   * the scalar loss must equal the mean of the per-position losses, a
     property that holds at any size;
   * dW (a sum over all positions) is compared in full on a T-truncated run
@@ -46,7 +47,8 @@ def _inputs(name, T=None):
 
 def _sample_rows(T, chunk, n=64, seed=0):
     rng = np.random.default_rng(seed)
-    fixed = [0, T - 1, chunk - 1, chunk, min(T - 1, 2 * chunk - 1)]
+    G = min(4, max(1, 4096 // chunk))  # chunks per backward group (include/kd.h)
+    fixed = [0, T - 1, chunk - 1, chunk, min(T - 1, 2 * chunk - 1), G * chunk - 1, G * chunk]
     rows = set(int(r) for r in fixed if 0 <= r < T)
     while len(rows) < n:
         rows.add(int(rng.integers(T)))
@@ -77,6 +79,15 @@ def test_full_size_sampled_positions(cuda_dev, name):
     np.testing.assert_allclose(rows_g[S], L_o, rtol=LOSS_RTOL, atol=1e-4)
     assert abs(rows_g[S].mean() - L_o.mean()) <= LOSS_RTOL * abs(L_o.mean())
     assert frob(dH[St].cpu().numpy(), dH_o) <= GRAD_RTOL
+    # the single call (no recompute) on the same positions
+    del dH
+    l1, lse1, rows1, dH1, dW1 = kd.fused_kl_fwdbwd(H, W, ids, logp, chunk, want_rows=True)
+    torch.cuda.synchronize()
+    r1 = rows1.cpu().numpy().astype(np.float64)
+    assert abs(l1.item() - r1.mean()) <= 1e-6 * abs(r1.mean())
+    np.testing.assert_allclose(lse1.cpu().numpy()[S], lse_o, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(r1[S], L_o, rtol=LOSS_RTOL, atol=1e-4)
+    assert frob(dH1[St].cpu().numpy(), dH_o) <= GRAD_RTOL
 
 
 @pytest.mark.parametrize("name", ["llama3b", "gptoss20b", "long"])

@@ -148,13 +148,16 @@ def test_grad_scale_and_accumulate(cuda_dev):
 
 @pytest.mark.parametrize("name", ["llama3b", "gptoss20b"])
 def test_full_width_truncated_run(cuda_dev, gemm_tiles, name):
-    """Full d, V and chunk of the workloads, T = 2 chunks + a ragged tail of
-    37: every element of dW and dH against the oracle."""
+    """Full d, V and chunk of the workloads, T = one full group of chunks
+    plus a ragged second group of 37 positions (G = clamp(4096 / chunk, 1, 4)
+    as include/kd.h states): every element of dW and dH against the
+    oracle."""
     if gemm_tiles != ("1", None):
         pytest.skip("full-width check runs in the default tile configuration")
     c = synth.CONFIGS[name]
     chunk = c["chunk"]
-    Tp = 2 * chunk + 37
+    G = min(4, max(1, 4096 // chunk))
+    Tp = G * chunk + 37
     H, W = synth.student(Tp, c["d"], c["V"], c["seed"], device=cuda_dev)
     ids, logp = synth.synthetic_cache(Tp, c["V"], c["K"], c["seed"])
     ids, logp = ids.to(cuda_dev), logp.to(cuda_dev)
