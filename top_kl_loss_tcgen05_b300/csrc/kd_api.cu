@@ -357,6 +357,98 @@ int parse_opts(const kd_kl_options* o, LossOpts* out) {
 
 const uint8_t* mask_at(const LossOpts& o, int64_t row0) { return o.mask ? o.mask + row0 : nullptr; }
 
+// Typed views of the fused-loss workspace (header words and the per-group
+// buffers of fused_layout).
+struct FusedWs {
+  int* status;
+  int* counter;   // tile counter of the GEMM launches
+  double* acc;    // fp64 loss accumulator
+  unsigned* done; // finished blocks of the current merge launch
+  float* scale;   // the backward's per-position gradient factor
+  int* ids_sorted;
+  float* p_sorted;
+  int* cnt;
+  float* ent;
+  float* zK;
+  double* bsum;
+  float* part_m;
+  float* part_s;
+  __nv_bfloat16* dz;
+  __nv_bfloat16* hct;
+};
+
+FusedWs fused_ws(void* ws, const Layout& L) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  FusedWs f;
+  f.status = reinterpret_cast<int*>(w);
+  f.counter = reinterpret_cast<int*>(w + kCounterOffset);
+  f.acc = reinterpret_cast<double*>(w + kAccOffset);
+  f.done = reinterpret_cast<unsigned*>(w + kDoneOffset);
+  f.scale = reinterpret_cast<float*>(w + kScaleOffset);
+  f.ids_sorted = reinterpret_cast<int*>(w + L.ids_sorted);
+  f.p_sorted = reinterpret_cast<float*>(w + L.p_sorted);
+  f.cnt = reinterpret_cast<int*>(w + L.cnt);
+  f.ent = reinterpret_cast<float*>(w + L.ent);
+  f.zK = reinterpret_cast<float*>(w + L.zK);
+  f.bsum = reinterpret_cast<double*>(w + L.block_sums);
+  f.part_m = reinterpret_cast<float*>(w + L.part_m);
+  f.part_s = reinterpret_cast<float*>(w + L.part_s);
+  f.dz = reinterpret_cast<__nv_bfloat16*>(w + L.dz);
+  f.hct = reinterpret_cast<__nv_bfloat16*>(w + L.hct);
+  return f;
+}
+
+// The logits GEMM z = H_g W^T of a call: tile shape and width (the default
+// for this GEMM, unless KD_GEMM_WIDE forces one), 1/tau for the epilogue,
+// and the tensor map of W (K-major B), shared by every group.
+int logits_setup(GemmArgs& a, int wide_default, float inv_tau, const void* W, int64_t d, int64_t V) {
+  std::memset(&a, 0, sizeof(a));
+  a.cta2 = gemm_cta2();
+  a.wide = gemm_wide(wide_default);
+  a.zscale = inv_tau;
+  if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
+                    gemm_b_box_rows(a.cta2)) != cudaSuccess)
+    return KD_ERR_UNSUPPORTED;
+  return KD_OK;
+}
+
+// The logits GEMM of one group of positions [g0, g0 + rows): the tensor map
+// of the group's H rows (K-major A), that of the dz buffer when the epilogue
+// stores a tile (store_dz), the problem shape, and the teacher-side arrays
+// and partial-statistics buffers the epilogues read or write.
+int logits_group(GemmArgs& a, const Layout& L, const FusedWs& f, const __nv_bfloat16* Hb, int64_t g0, int rows,
+                 int64_t d, int64_t V, bool store_dz) {
+  if (encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + g0 * d, (uint64_t)d, (uint64_t)rows,
+                    (uint64_t)d * 2, kBK, kBM) != cudaSuccess)
+    return KD_ERR_UNSUPPORTED;
+  if (store_dz && encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f.dz, (uint64_t)V, (uint64_t)rows,
+                                (uint64_t)L.ldz * 2, 64, 32) != cudaSuccess)
+    return KD_ERR_UNSUPPORTED;
+  Problem& P = a.pr[0];
+  P.m_blocks = (int)ceil_div(rows, gemm_tile_rows(a.cta2));
+  P.n_blocks = (int)ceil_div(V, gemm_tile_cols(a.cta2, a.wide));
+  P.k_blocks = (int)ceil_div(d, kBK);
+  P.a_mn = 0; P.b_mn = 0; P.M = rows; P.N = (int)V;
+  P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
+  a.nprob = 1;
+  a.total_tiles = P.m_blocks * P.n_blocks;
+  a.rows = rows; a.S = (int)L.S; a.V = (int)V; a.Kp = L.Kp;
+  a.ids_sorted = f.ids_sorted; a.p_sorted = f.p_sorted; a.cnt = f.cnt;
+  a.zK = f.zK; a.part_m = f.part_m; a.part_s = f.part_s;
+  a.status = f.status;
+  a.tile_counter = f.counter;
+  return KD_OK;
+}
+
+// Teacher side of one group: p renormalised over K (with 1/tau), entropy,
+// and the (id, p) list sorted by id.
+cudaError_t prep_group(const int32_t* ids, const float* logp, int64_t g0, int rows, int32_t K, int64_t V,
+                       const Layout& L, float inv_tau, const FusedWs& f, cudaStream_t s) {
+  ProfScope ps(K_PREP, s);
+  return launch_prep(ids + g0 * K, logp + g0 * K, rows, K, (int)V, L.Kp, inv_tau, f.ids_sorted, f.p_sorted, f.cnt,
+                     f.ent, f.status, s);
+}
+
 }  // namespace
 
 }  // namespace kd
@@ -421,62 +513,24 @@ int kd_fused_kl_fwd_ex(const void* H, const void* W, const int32_t* ids, const f
   if (sms <= 0) return KD_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout L = fused_layout(d, V, K, chunk);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  int* status = reinterpret_cast<int*>(w);
-  double* acc = reinterpret_cast<double*>(w + kAccOffset);
-  unsigned* done = reinterpret_cast<unsigned*>(w + kDoneOffset);
-  int* ids_sorted = reinterpret_cast<int*>(w + L.ids_sorted);
-  float* p_sorted = reinterpret_cast<float*>(w + L.p_sorted);
-  int* cnt = reinterpret_cast<int*>(w + L.cnt);
-  float* ent = reinterpret_cast<float*>(w + L.ent);
-  float* zK = reinterpret_cast<float*>(w + L.zK);
-  double* bsum = reinterpret_cast<double*>(w + L.block_sums);
-  float* part_m = reinterpret_cast<float*>(w + L.part_m);
-  float* part_s = reinterpret_cast<float*>(w + L.part_s);
+  const FusedWs f = fused_ws(ws, L);
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
   // The merge kernels count finished blocks in the workspace header; the
   // count returns to 0 after every launch, and starts there for this call.
-  cudaError_t e = cudaMemsetAsync(done, 0, sizeof(unsigned), s);
+  cudaError_t e = cudaMemsetAsync(f.done, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return cuda_status(e);
 
   GemmArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.cta2 = gemm_cta2();
-  a.wide = gemm_wide(1);
-  a.zscale = o.inv_tau;
-  const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
-  if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
-                    BR) != cudaSuccess)
-    return KD_ERR_UNSUPPORTED;
+  if ((st = logits_setup(a, 1, o.inv_tau, W, d, V)) != KD_OK) return st;
   // Positions go through in groups of G chunks (one GEMM launch per group:
   // more tiles per launch, fewer launches; the group is the unit the
   // workspace is sized for).
   const int64_t gchunk = L.G * chunk;
   for (int64_t c0 = 0; c0 < T; c0 += gchunk) {
     const int rows = (int)((T - c0) < gchunk ? (T - c0) : gchunk);
-    {
-      ProfScope ps(K_PREP, s);
-      e = launch_prep(ids + c0 * K, logp + c0 * K, rows, K, (int)V, L.Kp, o.inv_tau, ids_sorted, p_sorted, cnt, ent,
-                      status, s);
-    }
+    e = prep_group(ids, logp, c0, rows, K, V, L, o.inv_tau, f, s);
     if (e != cudaSuccess) return cuda_status(e);
-    if (encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + c0 * d, (uint64_t)d, (uint64_t)rows,
-                      (uint64_t)d * 2, kBK, kBM) != cudaSuccess)
-      return KD_ERR_UNSUPPORTED;
-    Problem& P = a.pr[0];
-    P.m_blocks = (int)ceil_div(rows, TR);
-    P.n_blocks = (int)ceil_div(V, gemm_tile_cols(a.cta2, a.wide));
-    P.k_blocks = (int)ceil_div(d, kBK);
-    P.a_mn = 0; P.b_mn = 0;
-    P.M = rows; P.N = (int)V;
-    P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0;
-    a.nprob = 1;
-    a.total_tiles = P.m_blocks * P.n_blocks;
-    a.rows = rows; a.S = (int)L.S; a.V = (int)V; a.Kp = L.Kp;
-    a.ids_sorted = ids_sorted; a.p_sorted = p_sorted; a.cnt = cnt;
-    a.zK = zK; a.part_m = part_m; a.part_s = part_s;
-    a.status = status;
-    a.tile_counter = reinterpret_cast<int*>(w + kCounterOffset);
+    if ((st = logits_group(a, L, f, Hb, c0, rows, d, V, false)) != KD_OK) return st;
     {
       ProfScope ps(K_LOGITS_FWD, s);
       e = launch_logits_fwd(a, sms, s);
@@ -484,13 +538,13 @@ int kd_fused_kl_fwd_ex(const void* H, const void* W, const int32_t* ids, const f
     if (e != cudaSuccess) return cuda_status(e);
     {
       ProfScope ps(K_MERGE, s);
-      e = launch_merge(part_m, part_s, (int)L.S, rows, ent, p_sorted, zK, cnt, L.Kp, mask_at(o, c0), lse + c0,
-                       loss_rows ? loss_rows + c0 : nullptr, bsum, done, acc, c0 == 0, s);
+      e = launch_merge(f.part_m, f.part_s, (int)L.S, rows, f.ent, f.p_sorted, f.zK, f.cnt, L.Kp, mask_at(o, c0),
+                       lse + c0, loss_rows ? loss_rows + c0 : nullptr, f.bsum, f.done, f.acc, c0 == 0, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
   }
   ProfScope ps(K_FINALIZE, s);
-  return cuda_status(launch_finalize(acc, T, o.mask, o.mean_over_mask, loss, s));
+  return cuda_status(launch_finalize(f.acc, T, o.mask, o.mean_over_mask, loss, s));
 }
 
 int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
@@ -513,77 +567,39 @@ int kd_fused_kl_bwd_ex(const void* H, const void* W, const int32_t* ids, const f
   if (sms <= 0) return KD_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout L = fused_layout(d, V, K, chunk);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  int* status = reinterpret_cast<int*>(w);
-  float* wscale = reinterpret_cast<float*>(w + kScaleOffset);
-  int* ids_sorted = reinterpret_cast<int*>(w + L.ids_sorted);
-  float* p_sorted = reinterpret_cast<float*>(w + L.p_sorted);
-  int* cnt = reinterpret_cast<int*>(w + L.cnt);
-  float* ent = reinterpret_cast<float*>(w + L.ent);
-  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(w + L.dz);
+  const FusedWs f = fused_ws(ws, L);
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
-  int* counter = reinterpret_cast<int*>(w + kCounterOffset);
-  __nv_bfloat16* hct = reinterpret_cast<__nv_bfloat16*>(w + L.hct);
 
   // s = grad_scale * (*grad_scale_dev) * 1/tau (* 1/N), on the device.
   cudaError_t e;
   {
     ProfScope ps(K_GRAD_SCALE, s);
-    e = launch_grad_scale(grad_scale, grad_scale_dev, o.inv_tau, o.mask, T, o.mean_over_mask, wscale, s);
+    e = launch_grad_scale(grad_scale, grad_scale_dev, o.inv_tau, o.mask, T, o.mean_over_mask, f.scale, s);
   }
   if (e != cudaSuccess) return cuda_status(e);
-  GemmArgs az, ag;
-  std::memset(&az, 0, sizeof(az));
-  az.cta2 = gemm_cta2();
-  az.wide = gemm_wide(0);
-  az.zscale = o.inv_tau;
-  const int TR = gemm_tile_rows(az.cta2), BR = gemm_b_box_rows(az.cta2);
   // W: K-major B of the logits GEMM, M-major A of the dH^T GEMM.
-  if (encode_map_2d(&az.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
-                    BR) != cudaSuccess)
-    return KD_ERR_UNSUPPORTED;
-  st = grad_setup(ag, W, dW, d, V, status, counter);
-  if (st != KD_OK) return st;
+  GemmArgs az, ag;
+  if ((st = logits_setup(az, 0, o.inv_tau, W, d, V)) != KD_OK) return st;
+  if ((st = grad_setup(ag, W, dW, d, V, f.status, f.counter)) != KD_OK) return st;
 
   // One group of G chunks at a time: prep, the recompute GEMM writing the
   // group's dz, then dH and dW of the group.
   const int64_t gchunk = L.G * chunk;
   for (int64_t g0 = 0; g0 < T; g0 += gchunk) {
     const int grows = (int)((T - g0) < gchunk ? (T - g0) : gchunk);
-    {
-      ProfScope ps(K_PREP, s);
-      e = launch_prep(ids + g0 * K, logp + g0 * K, grows, K, (int)V, L.Kp, o.inv_tau, ids_sorted, p_sorted, cnt, ent,
-                      status, s);
-    }
+    e = prep_group(ids, logp, g0, grows, K, V, L, o.inv_tau, f, s);
     if (e != cudaSuccess) return cuda_status(e);
     // Recompute the group's logits; the epilogue writes dz (bf16).
-    if (encode_map_2d(&az.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + g0 * d, (uint64_t)d, (uint64_t)grows,
-                      (uint64_t)d * 2, kBK, kBM) != cudaSuccess ||
-        encode_map_2d(&az.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
-                      (uint64_t)L.ldz * 2, 64, 32) != cudaSuccess)
-      return KD_ERR_UNSUPPORTED;
-    {
-      Problem& P = az.pr[0];
-      P.m_blocks = (int)ceil_div(grows, TR);
-      P.n_blocks = (int)ceil_div(V, gemm_tile_cols(az.cta2, az.wide));
-      P.k_blocks = (int)ceil_div(d, kBK);
-      P.a_mn = 0; P.b_mn = 0; P.M = grows; P.N = (int)V;
-      P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
-      az.nprob = 1;
-      az.total_tiles = P.m_blocks * P.n_blocks;
-      az.rows = grows; az.V = (int)V; az.Kp = L.Kp;
-      az.ids_sorted = ids_sorted; az.p_sorted = p_sorted; az.cnt = cnt;
-      az.lse = lse + g0; az.scale = 1.f; az.dscale = wscale;
-      az.mask = mask_at(o, g0);
-      az.status = status;
-      az.tile_counter = counter;
-    }
+    if ((st = logits_group(az, L, f, Hb, g0, grows, d, V, true)) != KD_OK) return st;
+    az.lse = lse + g0; az.scale = 1.f; az.dscale = f.scale;
+    az.mask = mask_at(o, g0);
     {
       ProfScope ps(K_LOGITS_DZ, s);
       e = launch_logits_dz(az, sms, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
-    st = grad_group(ag, L, Hb, dz, hct, dH, o.dH_bf16, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms, s);
+    st = grad_group(ag, L, Hb, f.dz, f.hct, dH, o.dH_bf16, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms,
+                    s);
     if (st != KD_OK) return st;
   }
   return KD_OK;
@@ -611,42 +627,19 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
   if (sms <= 0) return KD_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout L = fused_layout(d, V, K, chunk);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  int* status = reinterpret_cast<int*>(w);
-  int* counter = reinterpret_cast<int*>(w + kCounterOffset);
-  double* acc = reinterpret_cast<double*>(w + kAccOffset);
-  unsigned* done = reinterpret_cast<unsigned*>(w + kDoneOffset);
-  float* wscale = reinterpret_cast<float*>(w + kScaleOffset);
-  int* ids_sorted = reinterpret_cast<int*>(w + L.ids_sorted);
-  float* p_sorted = reinterpret_cast<float*>(w + L.p_sorted);
-  int* cnt = reinterpret_cast<int*>(w + L.cnt);
-  float* ent = reinterpret_cast<float*>(w + L.ent);
-  float* zK = reinterpret_cast<float*>(w + L.zK);
-  double* bsum = reinterpret_cast<double*>(w + L.block_sums);
-  float* part_m = reinterpret_cast<float*>(w + L.part_m);
-  float* part_s = reinterpret_cast<float*>(w + L.part_s);
-  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(w + L.dz);
-  __nv_bfloat16* hct = reinterpret_cast<__nv_bfloat16*>(w + L.hct);
+  const FusedWs f = fused_ws(ws, L);
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
-  cudaError_t e = cudaMemsetAsync(done, 0, sizeof(unsigned), s);
+  cudaError_t e = cudaMemsetAsync(f.done, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return cuda_status(e);
   {
     ProfScope ps(K_GRAD_SCALE, s);
-    e = launch_grad_scale(grad_scale, grad_scale_dev, o.inv_tau, o.mask, T, o.mean_over_mask, wscale, s);
+    e = launch_grad_scale(grad_scale, grad_scale_dev, o.inv_tau, o.mask, T, o.mean_over_mask, f.scale, s);
   }
   if (e != cudaSuccess) return cuda_status(e);
 
   GemmArgs a, ag;
-  std::memset(&a, 0, sizeof(a));
-  a.cta2 = gemm_cta2();
-  a.wide = gemm_wide(1);
-  a.zscale = o.inv_tau;
-  const int TR = gemm_tile_rows(a.cta2), BR = gemm_b_box_rows(a.cta2);
-  if (encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, kBK,
-                    BR) != cudaSuccess)
-    return KD_ERR_UNSUPPORTED;
-  st = grad_setup(ag, W, dW, d, V, status, counter);
-  if (st != KD_OK) return st;
+  if ((st = logits_setup(a, 1, o.inv_tau, W, d, V)) != KD_OK) return st;
+  if ((st = grad_setup(ag, W, dW, d, V, f.status, f.counter)) != KD_OK) return st;
 
   // One group of G chunks at a time: the group's logits are computed once,
   // and kept only as e = exp((z - m_tile) / tau) (bf16, in the dz buffer)
@@ -654,30 +647,9 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
   const int64_t gchunk = L.G * chunk;
   for (int64_t g0 = 0; g0 < T; g0 += gchunk) {
     const int grows = (int)((T - g0) < gchunk ? (T - g0) : gchunk);
-    {
-      ProfScope ps(K_PREP, s);
-      e = launch_prep(ids + g0 * K, logp + g0 * K, grows, K, (int)V, L.Kp, o.inv_tau, ids_sorted, p_sorted, cnt, ent,
-                      status, s);
-    }
+    e = prep_group(ids, logp, g0, grows, K, V, L, o.inv_tau, f, s);
     if (e != cudaSuccess) return cuda_status(e);
-    if (encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Hb + g0 * d, (uint64_t)d, (uint64_t)grows,
-                      (uint64_t)d * 2, kBK, kBM) != cudaSuccess ||
-        encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
-                      (uint64_t)L.ldz * 2, 64, 32) != cudaSuccess)
-      return KD_ERR_UNSUPPORTED;
-    Problem& P = a.pr[0];
-    P.m_blocks = (int)ceil_div(grows, TR);
-    P.n_blocks = (int)ceil_div(V, gemm_tile_cols(a.cta2, a.wide));
-    P.k_blocks = (int)ceil_div(d, kBK);
-    P.a_mn = 0; P.b_mn = 0; P.M = grows; P.N = (int)V;
-    P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = 0; P.c_trans = 0;
-    a.nprob = 1;
-    a.total_tiles = P.m_blocks * P.n_blocks;
-    a.rows = grows; a.S = (int)L.S; a.V = (int)V; a.Kp = L.Kp;
-    a.ids_sorted = ids_sorted; a.p_sorted = p_sorted; a.cnt = cnt;
-    a.zK = zK; a.part_m = part_m; a.part_s = part_s;
-    a.status = status;
-    a.tile_counter = counter;
+    if ((st = logits_group(a, L, f, Hb, g0, grows, d, V, true)) != KD_OK) return st;
     {
       ProfScope ps(K_LOGITS_FWD_STORE, s);
       e = launch_logits_fwd_store(a, sms, s);
@@ -685,21 +657,22 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
     if (e != cudaSuccess) return cuda_status(e);
     {
       ProfScope ps(K_MERGE, s);
-      e = launch_merge(part_m, part_s, (int)L.S, grows, ent, p_sorted, zK, cnt, L.Kp, mask_at(o, g0), lse + g0,
-                       loss_rows ? loss_rows + g0 : nullptr, bsum, done, acc, g0 == 0, s);
+      e = launch_merge(f.part_m, f.part_s, (int)L.S, grows, f.ent, f.p_sorted, f.zK, f.cnt, L.Kp, mask_at(o, g0),
+                       lse + g0, loss_rows ? loss_rows + g0 : nullptr, f.bsum, f.done, f.acc, g0 == 0, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
     {
       ProfScope ps(K_DZ_FROM_EXP, s);
-      e = launch_dz_from_exp(dz, L.ldz, (int)V, (int)L.S, grows, part_m, lse + g0, ids_sorted, p_sorted, zK, cnt,
-                             L.Kp, 1.f, wscale, mask_at(o, g0), s);
+      e = launch_dz_from_exp(f.dz, L.ldz, (int)V, (int)L.S, grows, f.part_m, lse + g0, f.ids_sorted, f.p_sorted,
+                             f.zK, f.cnt, L.Kp, 1.f, f.scale, mask_at(o, g0), s);
     }
     if (e != cudaSuccess) return cuda_status(e);
-    st = grad_group(ag, L, Hb, dz, hct, dH, o.dH_bf16, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms, s);
+    st = grad_group(ag, L, Hb, f.dz, f.hct, dH, o.dH_bf16, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms,
+                    s);
     if (st != KD_OK) return st;
   }
   ProfScope ps(K_FINALIZE, s);
-  return cuda_status(launch_finalize(acc, T, o.mask, o.mean_over_mask, loss, s));
+  return cuda_status(launch_finalize(f.acc, T, o.mask, o.mean_over_mask, loss, s));
 }
 
 int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
