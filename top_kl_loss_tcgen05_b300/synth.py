@@ -122,8 +122,10 @@ def topk_logits(T: int, V: int, seed: int, device="cpu", row0: int = 0, rows: in
     The bias is -log(1 + ((v + o_t) mod V)), with o_t drawn uniformly per row.
     `row0`/`rows` give a slice of the full [T, V] matrix. Rows are drawn in
     blocks of 256, each from a generator seeded by (seed, first row of the
-    block), so a slice that starts on a block boundary holds the same values
-    as that part of the full draw.
+    block), so a slice that starts on a block boundary and ends on one (or at
+    T) holds the same values as that part of the full draw. Within a block
+    the per-row offsets are drawn after the noise, so a slice that ends
+    inside a block gets other offsets for its last rows.
     """
     if row0 % 256:
         raise ValueError("row0 must be a multiple of 256")
