@@ -125,3 +125,34 @@ def test_gpu_cache_to_file_and_back_to_the_device(cuda_dev, tmp_path):
     assert all(g[1].device.type == "cuda" for g in parts)
     assert torch.equal(torch.cat([g[1] for g in parts]), ids)
     assert torch.equal(torch.cat([g[2] for g in parts]), logp)
+
+
+def test_concurrent_reads_on_one_reader(tmp_path):
+    """kd_cache_read may run from several threads on one reader (pread, no
+    shared file offset): every thread gets exactly its own ranges."""
+    import threading
+
+    ids, logp = _cache(T=2000, V=5000, K=24)
+    p = tmp_path / "c.kdtopk"
+    with CacheWriter(p, 5000, 24) as w:
+        w.append(ids, logp)
+    errors = []
+    with CacheReader(p) as r:
+        def worker(seed):
+            try:
+                g = torch.Generator().manual_seed(seed)
+                for _ in range(200):
+                    r0 = int(torch.randint(0, 2000, (1,), generator=g))
+                    n = int(torch.randint(0, 2000 - r0 + 1, (1,), generator=g))
+                    i2, l2 = r.read(r0, n)
+                    if not (torch.equal(i2, ids[r0:r0 + n]) and torch.equal(l2, logp[r0:r0 + n])):
+                        errors.append((seed, r0, n))
+            except BaseException as e:  # reported in the test thread
+                errors.append(e)
+
+        threads = [threading.Thread(target=worker, args=(s,)) for s in range(8)]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+    assert not errors, errors[:3]
