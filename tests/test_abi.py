@@ -121,3 +121,39 @@ def test_fused_argument_errors(lib):
         _native.KD_ERR_INVALID_ARG
     assert bwd(P16, P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, ctypes.c_void_p(0x10004), P16, 0, ws,
                big, None) == _native.KD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("tau,over,bf", [(0.0, 0, 0), (-1.0, 0, 0), (float("inf"), 0, 0), (float("nan"), 0, 0),
+                                         (1e-45, 0, 0), (1.0, 2, 0), (1.0, 0, -1)])
+def test_invalid_loss_options_are_rejected_on_every_call(lib, tau, over, bf):
+    """Bad kd_kl_options (tau <= 0, not finite or so small that 1/tau
+    overflows; flags outside {0, 1}) come back as KD_ERR_INVALID_ARG from
+    all three _ex calls, before anything touches CUDA."""
+    ws = ctypes.c_void_p(0x100000)
+    big = 1 << 40
+    o = ctypes.byref(_native.KLOptions(tau, None, over, bf))
+    assert lib.kd_fused_kl_fwd_ex(P16, P16, P16, P16, 64, 64, 128, 4, 32, P16, P16, None, o, ws, big, None) == \
+        _native.KD_ERR_INVALID_ARG
+    assert lib.kd_fused_kl_bwd_ex(P16, P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, P16, P16, 0, o, ws, big,
+                                  None) == _native.KD_ERR_INVALID_ARG
+    assert lib.kd_fused_kl_fwdbwd_ex(P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, P16, P16, None, P16, P16, 0,
+                                     o, ws, big, None) == _native.KD_ERR_INVALID_ARG
+
+
+def test_single_call_and_teacher_argument_errors(lib):
+    ws = ctypes.c_void_p(0x100000)
+    big = 1 << 40
+    one = lib.kd_fused_kl_fwdbwd
+    assert one(P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, None, P16, None, P16, P16, 0, ws, big, None) == \
+        _native.KD_ERR_INVALID_ARG  # no loss output
+    assert one(P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, P16, P16, None, ctypes.c_void_p(0x10004), P16, 0,
+               ws, big, None) == _native.KD_ERR_UNSUPPORTED  # dH not 16-byte aligned
+    t = lib.kd_teacher_topk_cache
+    assert t(P16, P16, 0, 64, 128, 4, 32, P16, P16, ws, big, None) == _native.KD_ERR_INVALID_ARG  # T = 0
+    assert t(P16, P16, 8, 64, 128, 129, 32, P16, P16, ws, big, None) == _native.KD_ERR_INVALID_ARG  # K > V
+    assert t(P16, P16, 8, 60, 128, 4, 32, P16, P16, ws, big, None) == _native.KD_ERR_UNSUPPORTED  # d % 8
+    assert t(ctypes.c_void_p(0x10008), P16, 8, 64, 128, 4, 32, P16, P16, ws, big, None) == _native.KD_ERR_UNSUPPORTED
+    assert t(P16, P16, 8, 64, 128, 4, 32, P16, P16, None, big, None) == _native.KD_ERR_WORKSPACE
+    need = lib.kd_teacher_topk_workspace_size(64, 128, 4, 32)
+    assert need > 0
+    assert t(P16, P16, 8, 64, 128, 4, 32, P16, P16, ws, need - 1, None) == _native.KD_ERR_WORKSPACE
