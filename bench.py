@@ -5,12 +5,14 @@
 One step is one pass of the whole loss path over one batch: kd_fused_kl_fwd
 (teacher prep, logits GEMM with the online log-sum-exp and id gather in its
 epilogue, merge) and then kd_fused_kl_bwd (recompute GEMM with the dz
-epilogue, dH and dW GEMMs), chunk by chunk. The default workload is the
-Llama-3.2-3B-shaped projection (T=8192, d=3072, V=128256, K=100,
-chunk=1024) with synthetic inputs and a teacher cache built by
-kd_topk_cache from a perturbed-W teacher. The offline cache extraction is
-timed separately on its own workload ([8192, 201088] bf16 logits) and reported
-under "topk_extraction".
+epilogue, dH and dW GEMMs), chunk group by chunk group. The headline workload
+is the long-context projection (T=262144, d=2880, V=201088, K=100,
+chunk=4096), the largest of the loss workloads, with synthetic inputs and a
+teacher cache built by kd_topk_cache from a perturbed-W teacher. The other
+two loss workloads (Llama-3.2-3B- and GPT-OSS-20B-shaped) are timed in the
+same run and reported under "other_configs". The offline cache extraction is
+timed separately on its own workload ([8192, 201088] bf16 logits) and
+reported under "topk_extraction".
 
 Prints one JSON line (rank 0). Under torchrun each rank runs an independent
 replica on its own GPU (no collective on the data path); the barrier and the
@@ -77,15 +79,21 @@ def kernel_src_hash(files=None) -> str:
 
 
 def gemm_tiles_desc() -> str:
-    """The GEMM tile shapes this process runs (KD_GEMM_CTA2 / KD_GEMM_WIDE
-    override the per-kernel defaults)."""
-    if os.environ.get("KD_GEMM_CTA2") == "0":
+    """The GEMM tile shapes this process runs (the library's test switches,
+    kd_test_set_gemm_tiles, override the per-kernel defaults)."""
+    cta2, wide = _native.get_gemm_tiles()
+    if cta2 == 0:
         return "128x256 per CTA"
-    wide = os.environ.get("KD_GEMM_WIDE")
-    if wide in ("0", "1"):
-        return "%s per CTA pair (tcgen05 cta_group::2), every GEMM" % ("256x512" if wide == "1" else "256x256")
+    if wide in (0, 1):
+        return "%s per CTA pair (tcgen05 cta_group::2), every GEMM" % ("256x512" if wide == 1 else "256x256")
     return ("256x512 per CTA pair for every GEMM but the dz recompute, which uses 256x256 "
             "(tcgen05 cta_group::2)")
+
+
+def default_group(chunk: int) -> int:
+    """Chunks per GEMM launch under the library's default rule (kd.h: G =
+    clamp(4096 / chunk, 1, 4), integer division)."""
+    return max(1, min(4, 4096 // chunk))
 
 
 def ncu_traffic(kernel: str, workload: str):
@@ -404,18 +412,174 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def fused_roofline(prof, steps, T, d, V, peaks, peaks_src, clk, workload):
+    """Roofline of the dominant kernel of a fused-loss step: algorithmic flops
+    per launch (the kernel's per-step flops / its launches per step) over its
+    mean CUDA-event launch time. Reported against the sustained bf16 peak (the
+    kernel runs inside a long step), against the burst peak, and
+    clock-normalised: against the sustained peak scaled from the SM clock it
+    was measured at to this run's median SM clock."""
+    flops_per_step = {"logits_fwd_lse_gather": 2.0 * T * d * V, "logits_dz": 2.0 * T * d * V,
+                      "grad_dH_dW": 4.0 * T * d * V}
+    flops_per_launch = {k: f * steps / prof[k][0] for k, f in flops_per_step.items() if k in prof}
+    total_kernel_ms = sum(v[1] for v in prof.values())
+    kernels = {k: {"launches": n, "ms_per_step": t / steps, "share": t / total_kernel_ms if total_kernel_ms else 0.0}
+               for k, (n, t) in prof.items()}
+    for k in kernels:
+        if k in flops_per_launch:
+            n, t = prof[k]
+            kernels[k]["tflops"] = flops_per_launch[k] / (t / n * 1e-3) / 1e12
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
+    roof = None
+    if dom in flops_per_launch:
+        n, t = prof[dom]
+        achieved = flops_per_launch[dom] / (t / n * 1e-3) / 1e12
+        peak_tf = float(peaks["bf16_tflops_sustained"])
+        peak_burst = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf, "traffic": ncu_traffic(dom, workload), "kernel": dom,
+                "peak_kind": "bf16_tflops_sustained (%s)" % peaks_src,
+                "algorithmic_flops_per_launch": flops_per_launch[dom],
+                "peak_burst": peak_burst, "frac_burst": achieved / peak_burst}
+        peak_mhz = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
+        if clk and clk.get("sm_mhz") and peak_mhz:
+            roof.update({"sm_mhz": clk["sm_mhz"], "peak_sustained_sm_mhz": peak_mhz,
+                         "frac_clock_normalised": achieved / (peak_tf * clk["sm_mhz"] / peak_mhz),
+                         "clock_note": "frac_clock_normalised = achieved / (peak x this run's median SM MHz / "
+                                       "the median SM MHz the sustained peak was measured at)"})
+    return roof, kernels, sum(n for n, _ in prof.values())
+
+
+class FusedRun:
+    """Device buffers and the fused-loss step (kd_fused_kl_fwd then
+    kd_fused_kl_bwd, through the C ABI) of one workload."""
+
+    def __init__(self, name, dev):
+        self.name = name
+        self.dev = dev
+        wl = make_workload(name, dev)
+        self.wl = wl
+        self.T, self.d, self.V, self.K, self.chunk = wl["T"], wl["d"], wl["V"], wl["K"], wl["chunk"]
+        self.H, self.W, self.ids, self.logp = wl["H"], wl["W"], wl["ids"], wl["logp"]
+        self.ws = kd.fused_kl_workspace(self.d, self.V, self.K, self.chunk, dev)
+        self.lse = torch.empty(self.T, dtype=torch.float32, device=dev)
+        self.loss = torch.empty((), dtype=torch.float32, device=dev)
+        self.dH = torch.empty(self.T, self.d, dtype=torch.float32, device=dev)
+        self.dW = torch.empty(self.V, self.d, dtype=torch.float32, device=dev)
+        self.L = _native.lib()
+        self.stream = torch.cuda.current_stream(dev).cuda_stream
+
+    def fwd(self, Hx=None, idsx=None, logpx=None):
+        Hx = self.H if Hx is None else Hx
+        idsx = self.ids if idsx is None else idsx
+        logpx = self.logp if logpx is None else logpx
+        _native.check("kd_fused_kl_fwd", self.L.kd_fused_kl_fwd(
+            Hx.data_ptr(), self.W.data_ptr(), idsx.data_ptr(), logpx.data_ptr(), self.T, self.d, self.V, self.K,
+            self.chunk, self.loss.data_ptr(), self.lse.data_ptr(), None, self.ws.data_ptr(), self.ws.numel(),
+            self.stream))
+
+    def bwd(self, Hx=None, idsx=None, logpx=None):
+        Hx = self.H if Hx is None else Hx
+        idsx = self.ids if idsx is None else idsx
+        logpx = self.logp if logpx is None else logpx
+        _native.check("kd_fused_kl_bwd", self.L.kd_fused_kl_bwd(
+            Hx.data_ptr(), self.W.data_ptr(), idsx.data_ptr(), logpx.data_ptr(), self.lse.data_ptr(), self.T,
+            self.d, self.V, self.K, self.chunk, 1.0 / self.T, None, self.dH.data_ptr(), self.dW.data_ptr(), 0,
+            self.ws.data_ptr(), self.ws.numel(), self.stream))
+
+    def step(self, Hx=None, idsx=None, logpx=None):
+        self.fwd(Hx, idsx, logpx)
+        self.bwd(Hx, idsx, logpx)
+
+    def fwdbwd(self):
+        _native.check("kd_fused_kl_fwdbwd", self.L.kd_fused_kl_fwdbwd(
+            self.H.data_ptr(), self.W.data_ptr(), self.ids.data_ptr(), self.logp.data_ptr(), self.T, self.d, self.V,
+            self.K, self.chunk, 1.0 / self.T, None, self.loss.data_ptr(), self.lse.data_ptr(), None,
+            self.dH.data_ptr(), self.dW.data_ptr(), 0, self.ws.data_ptr(), self.ws.numel(), self.stream))
+
+    def io_gib(self):
+        ts = (self.H, self.W, self.ids, self.logp, self.lse, self.loss, self.dH, self.dW)
+        return sum(t.numel() * t.element_size() for t in ts) / 2**30
+
+    def check_status(self, where):
+        st = kd.read_device_status(self.ws)
+        if st != 0:
+            raise RuntimeError("device status %s %s" % (_native.status_string(st), where))
+
+    def peak_step(self):
+        """Peak device memory of one step (everything is allocated through torch)."""
+        torch.cuda.synchronize(self.dev)
+        torch.cuda.reset_peak_memory_stats(self.dev)
+        self.step()
+        torch.cuda.synchronize(self.dev)
+        return torch.cuda.max_memory_allocated(self.dev) / 2**30
+
+    def timed(self, steps, world):
+        """(elapsed ms max over ranks, per-kernel profile, clocks) of `steps`
+        back-to-back steps, bracketed by a barrier and synchronisations."""
+        clocks = ClockSampler(self.dev)
+        barrier(world)
+        torch.cuda.synchronize(self.dev)
+        clocks.start()
+        time.sleep(0.3)
+        _native.profile_begin()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        for _ in range(steps):
+            self.step()
+        ev1.record()
+        torch.cuda.synchronize(self.dev)
+        prof = _native.profile_end()
+        barrier(world)
+        clk = clocks.stop()
+        return max_over_ranks(ev0.elapsed_time(ev1), world), prof, clk
+
+
+def config_desc(run: FusedRun) -> dict:
+    G = default_group(run.chunk)
+    return {"workload": describe(run.name), "group": G, "rows_per_gemm_launch": G * run.chunk,
+            "group_note": "each GEMM launch covers a group of G chunks (the library's default group rule); the "
+                          "workspace holds one group's bf16 dz"}
+
+
+def measure_other(name, args, dev, peaks, peaks_src, world):
+    """tokens/s, TFLOP/s, % of the bf16 peaks, roofline and peak memory of one
+    more loss workload, timed like the headline (K steps after W warm-up)."""
+    run = FusedRun(name, dev)
+    peak_gib = run.peak_step()
+    for _ in range(args.warmup - 1):
+        run.step()
+    run.check_status("during warm-up (%s)" % name)
+    el_ms, prof, clk = run.timed(args.steps, world)
+    run.check_status("in the timed region (%s)" % name)
+    T, d, V = run.T, run.d, run.V
+    tflops = 8.0 * T * d * V * args.steps * world / (el_ms * 1e-3) / 1e12
+    roof, kernels, launches = fused_roofline(prof, args.steps, T, d, V, peaks, peaks_src, clk, name)
+    out = {"value": T * args.steps * world / (el_ms * 1e-3), "unit": "tokens/s", "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": el_ms / args.steps, "tflops": tflops,
+           "pct_bf16_peak": tflops / float(peaks["bf16_tflops_sustained"]),
+           "pct_bf16_peak_burst": tflops / float(peaks["bf16_tflops"]),
+           "peak_gib": peak_gib, "workspace_gib": run.ws.numel() / 2**30, "io_gib": run.io_gib(),
+           "config": config_desc(run), "roofline": roof, "gpu_launches": launches, "clocks": clk,
+           "kernels": kernels}
+    del run
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama3b", choices=["tiny", "llama3b", "gptoss20b", "long"])
+    ap.add_argument("--workload", default="long", choices=["tiny", "llama3b", "gptoss20b", "long"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-topk", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-fwdbwd", action="store_true", help="skip timing the single-call forward + backward")
     ap.add_argument("--no-teacher", action="store_true", help="skip timing the teacher-side cache")
+    ap.add_argument("--no-others", action="store_true", help="skip timing the other loss workloads")
     ap.add_argument("--topk-rows", type=int, default=None, help="rows of the top-K workload (default 8192)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -427,101 +591,34 @@ def main():
     peaks, peaks_src = load_peaks()
     _native.load()
 
-    wl = make_workload(args.workload, dev)
-    T, d, V, K, chunk = wl["T"], wl["d"], wl["V"], wl["K"], wl["chunk"]
-    H, W, ids, logp = wl["H"], wl["W"], wl["ids"], wl["logp"]
-    ws = kd.fused_kl_workspace(d, V, K, chunk, dev)
-    lse = torch.empty(T, dtype=torch.float32, device=dev)
-    loss = torch.empty((), dtype=torch.float32, device=dev)
-    dH = torch.empty(T, d, dtype=torch.float32, device=dev)
-    dW = torch.empty(V, d, dtype=torch.float32, device=dev)
-    L = _native.lib()
-    stream = torch.cuda.current_stream(dev).cuda_stream
-
-    def step(Hx=H, idsx=ids, logpx=logp):
-        _native.check("kd_fused_kl_fwd", L.kd_fused_kl_fwd(
-            Hx.data_ptr(), W.data_ptr(), idsx.data_ptr(), logpx.data_ptr(), T, d, V, K, chunk, loss.data_ptr(),
-            lse.data_ptr(), None, ws.data_ptr(), ws.numel(), stream))
-        _native.check("kd_fused_kl_bwd", L.kd_fused_kl_bwd(
-            Hx.data_ptr(), W.data_ptr(), idsx.data_ptr(), logpx.data_ptr(), lse.data_ptr(), T, d, V, K, chunk,
-            1.0 / T, None, dH.data_ptr(), dW.data_ptr(), 0, ws.data_ptr(), ws.numel(), stream))
-
-    # peak device memory of one step (everything is allocated through torch)
-    torch.cuda.synchronize(dev)
-    torch.cuda.reset_peak_memory_stats(dev)
-    step()
-    torch.cuda.synchronize(dev)
-    peak_gib = torch.cuda.max_memory_allocated(dev) / 2**30
-    ws_gib = ws.numel() / 2**30
-    io_gib = sum(t.numel() * t.element_size() for t in (H, W, ids, logp, lse, loss, dH, dW)) / 2**30
+    run = FusedRun(args.workload, dev)
+    T, d, V, K, chunk = run.T, run.d, run.V, run.K, run.chunk
+    H, W, ids, logp = run.H, run.W, run.ids, run.logp
+    peak_gib = run.peak_step()
+    ws_gib = run.ws.numel() / 2**30
+    io_gib = run.io_gib()
     for _ in range(args.warmup - 1):
-        step()
+        run.step()
     torch.cuda.synchronize(dev)
-    status = kd.read_device_status(ws)
-    if status != 0:
-        raise RuntimeError("device status %s during warm-up" % _native.status_string(status))
+    run.check_status("during warm-up")
 
     # ---- timed region (device-resident inputs)
-    clocks = ClockSampler(dev)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.3)
-    _native.profile_begin()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    for _ in range(args.steps):
-        step()
-    ev1.record()
-    torch.cuda.synchronize(dev)
-    prof = _native.profile_end()
-    barrier(world)
-    clk = clocks.stop()
-    el_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    el_ms, prof, clk = run.timed(args.steps, world)
     ms_step = el_ms / args.steps
     tokens_s = T * args.steps * world / (el_ms * 1e-3)
-    flops_step = 8.0 * T * d * V
-    tflops = flops_step * args.steps * world / (el_ms * 1e-3) / 1e12
+    tflops = 8.0 * T * d * V * args.steps * world / (el_ms * 1e-3) / 1e12
     peak_tf = float(peaks["bf16_tflops_sustained"])
-    status = kd.read_device_status(ws)
-    if status != 0:
-        raise RuntimeError("device status %s in the timed region" % _native.status_string(status))
-
-    # dominant kernel and its roofline (algorithmic flops per launch / mean
-    # launch time). Per step: logits 2TdV, recompute 2TdV, dH + dW 4TdV,
-    # spread over however many launches each kernel made.
-    flops_per_step = {"logits_fwd_lse_gather": 2.0 * T * d * V, "logits_dz": 2.0 * T * d * V,
-                      "grad_dH_dW": 4.0 * T * d * V}
-    flops_per_launch = {k: f * args.steps / prof[k][0] for k, f in flops_per_step.items() if k in prof}
-    total_kernel_ms = sum(v[1] for v in prof.values())
-    dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
-    kernels = {k: {"launches": n, "ms_per_step": t / args.steps, "share": t / total_kernel_ms if total_kernel_ms else 0.0}
-               for k, (n, t) in prof.items()}
-    roof = None
-    if dom in flops_per_launch:
-        n, t = prof[dom]
-        achieved = flops_per_launch[dom] / (t / n * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": achieved / peak_tf, "traffic": ncu_traffic(dom, args.workload), "kernel": dom,
-                "peak_kind": "bf16_tflops_sustained (%s)" % peaks_src,
-                "algorithmic_flops_per_launch": flops_per_launch[dom]}
-    for k in kernels:
-        if k in flops_per_launch:
-            n, t = prof[k]
-            kernels[k]["tflops"] = flops_per_launch[k] / (t / n * 1e-3) / 1e12
-    gpu_launches = sum(n for n, _ in prof.values())
+    run.check_status("in the timed region")
+    roof, kernels, gpu_launches = fused_roofline(prof, args.steps, T, d, V, peaks, peaks_src, clk, args.workload)
 
     # forward and backward separately (same calls, events between them)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    n_ph = min(args.steps, 5)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ph)]
     for e in evs:
         e[0].record()
-        _native.check("kd_fused_kl_fwd", L.kd_fused_kl_fwd(
-            H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K, chunk, loss.data_ptr(),
-            lse.data_ptr(), None, ws.data_ptr(), ws.numel(), stream))
+        run.fwd()
         e[1].record()
-        _native.check("kd_fused_kl_bwd", L.kd_fused_kl_bwd(
-            H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), lse.data_ptr(), T, d, V, K, chunk,
-            1.0 / T, None, dH.data_ptr(), dW.data_ptr(), 0, ws.data_ptr(), ws.numel(), stream))
+        run.bwd()
         e[2].record()
     torch.cuda.synchronize(dev)
     fwd_ms = sorted(e[0].elapsed_time(e[1]) for e in evs)[len(evs) // 2]
@@ -534,35 +631,28 @@ def main():
     # headline, which is the recompute path (8 T d V).
     fwdbwd = None
     if not args.no_fwdbwd:
-        def fb_step():
-            _native.check("kd_fused_kl_fwdbwd", L.kd_fused_kl_fwdbwd(
-                H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K, chunk, 1.0 / T, None,
-                loss.data_ptr(), lse.data_ptr(), None, dH.data_ptr(), dW.data_ptr(), 0, ws.data_ptr(), ws.numel(),
-                stream))
-
+        n_fb = min(args.steps, 10)
         for _ in range(args.warmup):
-            fb_step()
+            run.fwdbwd()
         torch.cuda.synchronize(dev)
         barrier(world)
         _native.profile_begin()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record()
-        for _ in range(args.steps):
-            fb_step()
+        for _ in range(n_fb):
+            run.fwdbwd()
         f1.record()
         torch.cuda.synchronize(dev)
         fprof = _native.profile_end()
-        fb_ms = max_over_ranks(f0.elapsed_time(f1), world) / args.steps
-        st = kd.read_device_status(ws)
-        if st != 0:
-            raise RuntimeError("device status %s in kd_fused_kl_fwdbwd" % _native.status_string(st))
+        fb_ms = max_over_ranks(f0.elapsed_time(f1), world) / n_fb
+        run.check_status("in kd_fused_kl_fwdbwd")
         fb_tot = sum(v[1] for v in fprof.values())
-        fwdbwd = {"value": T * world / (fb_ms * 1e-3), "unit": "tokens/s", "ms_per_step": fb_ms,
+        fwdbwd = {"value": T * world / (fb_ms * 1e-3), "unit": "tokens/s", "ms_per_step": fb_ms, "steps": n_fb,
                   "tflops_executed": 6.0 * T * d * V * world / (fb_ms * 1e-3) / 1e12,
                   "pct_bf16_peak_executed": 6.0 * T * d * V / (fb_ms * 1e-3) / 1e12 / peak_tf,
                   "flops_basis": "6*T*d*V: the projection is computed once per chunk, no recompute",
                   "gpu_launches": sum(n for n, _ in fprof.values()),
-                  "kernels": {k: {"launches": n, "ms_per_step": t / args.steps, "share": t / fb_tot if fb_tot else 0.0}
+                  "kernels": {k: {"launches": n, "ms_per_step": t / n_fb, "share": t / fb_tot if fb_tot else 0.0}
                               for k, (n, t) in fprof.items()}}
 
     # ---- end to end through the public API with host buffers
@@ -587,8 +677,8 @@ def main():
 
         def serial_step():
             h2d(0, cur)
-            step(*bufs[0])
-            out.copy_(loss, non_blocking=True)
+            run.step(*bufs[0])
+            out.copy_(run.loss, non_blocking=True)
             cur.synchronize()
             return float(out)
 
@@ -599,8 +689,8 @@ def main():
             for i in range(n):
                 b = i & 1
                 cur.wait_event(ready)
-                step(*bufs[b])
-                out.copy_(loss, non_blocking=True)
+                run.step(*bufs[b])
+                out.copy_(run.loss, non_blocking=True)
                 if i + 1 < n:
                     ready = h2d(b ^ 1, side)  # buffer b ^ 1 was last read by step i - 1, which has finished
                 cur.synchronize()
@@ -610,7 +700,7 @@ def main():
             serial_step()
         run_pipelined(2)
         torch.cuda.synchronize(dev)
-        n_e2e = max(3, args.steps // 2)
+        n_e2e = max(3, min(8, args.steps // 2))
         barrier(world)
         t0 = time.perf_counter()
         run_pipelined(n_e2e)
@@ -627,12 +717,28 @@ def main():
                        "a side stream while the current step runs (a prefetching loader). serial_value: copy, "
                        "step and read-back one after another. W (LM-head parameter), dH and dW stay on the "
                        "device"}
+        del bufs, Hh, ih, lh
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:  # a reported baseline at N=1 only
+        cpu = cpu_baseline(run.wl)
+    cfg = config_desc(run)
+    cfg.update({"parallelism": "replicas" if world > 1 else "1 gpu",
+                "l2": "inputs larger than L2 (W alone is %.0f MB)" % (V * d * 2 / 1e6),
+                "teacher_cache": "kd_topk_cache of fp32 perturbed-W teacher logits",
+                "gemm_tiles": gemm_tiles_desc()})
+    del run, H, W, ids, logp
+    torch.cuda.empty_cache()
+
+    # ---- the other loss workloads, each timed like the headline
+    others = {}
+    if not args.no_others:
+        for name in ("llama3b", "gptoss20b", "long"):
+            if name != args.workload:
+                others[name] = measure_other(name, args, dev, peaks, peaks_src, world)
 
     topk = None if args.no_topk else bench_topk(dev, peaks, rows=args.topk_rows)
     teacher = None if args.no_teacher else bench_teacher(dev, peaks)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:  # a reported baseline at N=1 only
-        cpu = cpu_baseline(wl)
 
     if rank == 0:
         line = {
@@ -640,15 +746,14 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "tflops": tflops, "pct_bf16_peak": tflops / peak_tf,
-            "pct_bf16_peak_basis": "8*T*d*V flops per step vs bf16_tflops_sustained (%s)" % peaks_src,
+            "pct_bf16_peak_burst": tflops / float(peaks["bf16_tflops"]),
+            "pct_bf16_peak_basis": "8*T*d*V flops per step vs bf16_tflops_sustained and bf16_tflops (burst) "
+                                   "(%s)" % peaks_src,
             "peak_gib": peak_gib, "workspace_gib": ws_gib, "io_gib": io_gib, "phases": phases,
-            "config": {"workload": describe(args.workload), "parallelism": "replicas" if world > 1 else "1 gpu",
-                       "l2": "inputs larger than L2 (W alone is %.0f MB)" % (V * d * 2 / 1e6),
-                       "teacher_cache": "kd_topk_cache of fp32 perturbed-W teacher logits",
-                       "gemm_tiles": gemm_tiles_desc()},
+            "config": cfg,
             "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
-            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "topk_extraction": topk, "fused_fwdbwd": fwdbwd,
-            "teacher_topk": teacher,
+            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "other_configs": others or None,
+            "topk_extraction": topk, "fused_fwdbwd": fwdbwd, "teacher_topk": teacher,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -150,8 +150,12 @@ KD_API int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_
  * Scratch comes from a fixed 4096-byte array in device memory owned by
  * libkd. Every GPU that loads the library holds it until the process exits.
  * The call allocates nothing.
+ *  - Arguments are checked, as kd_topk_cache checks them, before anything is
+ *    enqueued; a refused call leaves the stream untouched.
  *  - The first call on a device looks up that array's device address
- *    (cudaGetSymbolAddress). Make that first call before any stream capture.
+ *    (cudaGetSymbolAddress) and keeps it. Make that first call before any
+ *    stream capture. The lookup is repeated when the device's context has
+ *    changed since (after cudaDeviceReset, for example).
  *  - Each call clears the array on `stream`. Calls that overlap on the GPU
  *    (unordered streams) share the array and race on it.
  *  - If the workspace that kd_topk_cache would need exceeds the array, the call
@@ -173,16 +177,24 @@ KD_API int kd_topk_cache_noalloc(const void* logits, int32_t dtype, int64_t T, i
  *         gradient does. An id outside [0, V) is ignored and sets
  *         KD_ERR_BAD_ID in the status word.
  *   chunk positions per chunk, 1 <= chunk. The chunk size changes results
- *         only by fp32 rounding order. The backward runs its dH/dW GEMM over
- *         groups of G = clamp(4096 / chunk, 1, 4) chunks (integer division),
- *         and the workspace holds one group's bf16 dz: about
- *         2 * G * chunk * V bytes, at most 8 * chunk * V.
+ *         only by fp32 rounding order. Each GEMM launch covers a group of
+ *         G chunks (G * chunk positions): G = kd_kl_options.group when that
+ *         is set, else clamp(4096 / chunk, 1, 4) (integer division). Grouping
+ *         makes the dW tiles' contraction longer, so their fp32
+ *         read-modify-write of dW is paid once per group. The workspace holds
+ *         one group's bf16 dz: about 2 * G * chunk * V bytes. A caller who
+ *         sizes `chunk` to bound memory passes group = 1 (through the _ex
+ *         calls) and gets about 2 * chunk * V.
  *   Requires d % 8 == 0 (16-byte rows for TMA), 16-byte aligned H and W,
  *   1 <= K <= 4096, 1 <= V < 2^31.
- *   Workspace: kd_fused_kl_workspace_size(d, V, K, chunk) bytes. It does not
- *   depend on T; one workspace serves all three calls.
+ *   Workspace: kd_fused_kl_workspace_size(d, V, K, chunk) bytes for the
+ *   default group, kd_fused_kl_workspace_size_ex(d, V, K, chunk, group) for
+ *   an explicit one (group = 0 is the default). It does not depend on T; one
+ *   workspace serves all three calls made with the same group. Both return 0
+ *   for a non-positive size or a negative group.
  */
 KD_API size_t kd_fused_kl_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk);
+KD_API size_t kd_fused_kl_workspace_size_ex(int64_t d, int64_t V, int32_t K, int64_t chunk, int32_t group);
 
 /* Forward. Writes:
  *   loss       device float32 scalar: (1/T) sum_t L_t.
@@ -259,14 +271,19 @@ KD_API int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, 
  *                   so grad_scale is d objective / d loss (1 for the loss
  *                   alone). N is counted on the device; nothing synchronises.
  *   dH_bf16         1: dH is written as bf16 [T, d] (dH points to bf16).
- * An invalid option (tau <= 0 or not finite, flags outside {0, 1}) returns
- * KD_ERR_INVALID_ARG.
+ *   group           chunks per GEMM launch (see `chunk` above); 0 = the
+ *                   default rule. The workspace must then be at least
+ *                   kd_fused_kl_workspace_size_ex(d, V, K, chunk, group).
+ *                   group * chunk must not exceed 2^24 (KD_ERR_UNSUPPORTED).
+ * An invalid option (tau <= 0 or not finite, flags outside {0, 1}, a
+ * negative group) returns KD_ERR_INVALID_ARG.
  */
 typedef struct kd_kl_options {
   float temperature;
   const uint8_t* mask;
   int32_t mean_over_mask;
   int32_t dH_bf16;
+  int32_t group;
 } kd_kl_options;
 
 KD_API int kd_fused_kl_fwd_ex(const void* H, const void* W, const int32_t* ids, const float* logp,

@@ -38,6 +38,23 @@ KD_API int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64
  * the context stays usable. Read the word with kd_read_device_status. */
 KD_API int kd_test_wait_timeout(int64_t limit_ns, void* ws, void* stream);
 
+/* Process-wide switches of the kernels a call runs, for tests and
+ * measurements. Production callers leave them at their defaults; nothing in
+ * the environment changes them.
+ * kd_test_set_gemm_tiles: cta2 = -1 (default: CTA-pair tiles), 0 (one CTA
+ *   per 128 x 256 tile) or 1 (CTA pairs); wide = -1 (default: each GEMM's
+ *   own width), 0 (every pair GEMM 256 x 256) or 1 (every pair GEMM
+ *   256 x 512). Calls already enqueued keep the shape they were set up with;
+ *   calls made afterwards, from any thread, use the new one. Values outside
+ *   {-1, 0, 1} return KD_ERR_INVALID_ARG and change nothing.
+ * kd_test_get_gemm_tiles: the current switch values (-1 = default).
+ * kd_test_set_topk_force_exact: on = 1 sends every row of kd_topk_cache and
+ *   kd_teacher_topk_cache through the exact radix selection (the path that
+ *   otherwise handles overflowing rows); 0 restores the default. */
+KD_API int kd_test_set_gemm_tiles(int32_t cta2, int32_t wide);
+KD_API int kd_test_get_gemm_tiles(int32_t* cta2, int32_t* wide);
+KD_API int kd_test_set_topk_force_exact(int32_t on);
+
 #ifdef __cplusplus
 }
 #endif

@@ -157,3 +157,69 @@ def test_single_call_and_teacher_argument_errors(lib):
     need = lib.kd_teacher_topk_workspace_size(64, 128, 4, 32)
     assert need > 0
     assert t(P16, P16, 8, 64, 128, 4, 32, P16, P16, ws, need - 1, None) == _native.KD_ERR_WORKSPACE
+
+
+def test_group_option_sets_the_workspace(lib):
+    """kd_fused_kl_workspace_size_ex grows with chunk * group; group = 1 makes
+    chunk alone the unit (one chunk's dz), and group = 0 is the default rule."""
+    f = lib.kd_fused_kl_workspace_size_ex
+    d, V, K = 2880, 201088, 100
+    for chunk in (256, 1024, 2048):
+        n1 = f(d, V, K, chunk, 1)
+        dz1 = chunk * V * 2
+        assert dz1 < n1 < 1.05 * dz1 + 64 * 2**20
+        for G in (2, 3, 4, 8):
+            nG = f(d, V, K, chunk, G)
+            assert G * dz1 < nG < 1.05 * G * dz1 + 64 * 2**20, (chunk, G)
+        assert f(d, V, K, chunk, 0) == lib.kd_fused_kl_workspace_size(d, V, K, chunk)
+    assert 1.9 < f(d, V, K, 2048, 1) / f(d, V, K, 1024, 1) < 2.1
+    assert f(d, V, K, 1024, -1) == 0
+
+
+def test_invalid_group_is_rejected_and_workspace_follows_the_group(lib):
+    ws = ctypes.c_void_p(0x100000)
+    o_neg = ctypes.byref(_native.KLOptions(1.0, None, 0, 0, -1))
+    assert lib.kd_fused_kl_fwd_ex(P16, P16, P16, P16, 64, 64, 128, 4, 32, P16, P16, None, o_neg, ws, 1 << 40,
+                                  None) == _native.KD_ERR_INVALID_ARG
+    # a workspace sized for group 1 is too small for group 4
+    need1 = lib.kd_fused_kl_workspace_size_ex(64, 4096, 4, 256, 1)
+    o4 = ctypes.byref(_native.KLOptions(1.0, None, 0, 0, 4))
+    assert lib.kd_fused_kl_fwd_ex(P16, P16, P16, P16, 64, 64, 4096, 4, 256, P16, P16, None, o4, ws, need1,
+                                  None) == _native.KD_ERR_WORKSPACE
+    # group * chunk beyond 2^24 rows per launch
+    o_big = ctypes.byref(_native.KLOptions(1.0, None, 0, 0, 1 << 20))
+    assert lib.kd_fused_kl_bwd_ex(P16, P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, P16, P16, 0, o_big, ws,
+                                  1 << 40, None) == _native.KD_ERR_UNSUPPORTED
+
+
+def test_test_switches_are_setters_not_environment(lib, monkeypatch):
+    """The tile-shape and exact-selection switches live behind kd_testing.h
+    setters; the environment does not change them."""
+    a, b = ctypes.c_int32(7), ctypes.c_int32(7)
+    monkeypatch.setenv("KD_GEMM_CTA2", "0")
+    monkeypatch.setenv("KD_GEMM_WIDE", "1")
+    assert lib.kd_test_get_gemm_tiles(ctypes.byref(a), ctypes.byref(b)) == 0
+    assert (a.value, b.value) == (-1, -1)
+    assert lib.kd_test_set_gemm_tiles(2, 0) == _native.KD_ERR_INVALID_ARG
+    assert lib.kd_test_set_gemm_tiles(0, -2) == _native.KD_ERR_INVALID_ARG
+    try:
+        assert lib.kd_test_set_gemm_tiles(0, 1) == 0
+        assert lib.kd_test_get_gemm_tiles(ctypes.byref(a), ctypes.byref(b)) == 0
+        assert (a.value, b.value) == (0, 1)
+    finally:
+        assert lib.kd_test_set_gemm_tiles(-1, -1) == 0
+    assert lib.kd_test_set_topk_force_exact(2) == _native.KD_ERR_INVALID_ARG
+    assert lib.kd_test_set_topk_force_exact(1) == 0 and lib.kd_test_set_topk_force_exact(0) == 0
+    with open(os.path.join(ROOT, "top_kl_loss_tcgen05_b300", "csrc", "kd_api.cu")) as f:
+        src = f.read()
+    assert re.findall(r'getenv\("([A-Z_]+)"\)', src) == ["KD_DEBUG"]
+
+
+def test_noalloc_refuses_before_touching_the_stream(lib):
+    """kd_topk_cache_noalloc runs kd_topk_cache's checks before anything is
+    enqueued: these refusals return without a CUDA call (no GPU here)."""
+    call = lib.kd_topk_cache_noalloc
+    assert call(ctypes.c_void_p(0x1001), 0, 4, 8, 8, 2, P16, P16, None) == _native.KD_ERR_UNSUPPORTED  # alignment
+    assert call(P16, 0, 4, 1 << 31, 1 << 31, 2, P16, P16, None) == _native.KD_ERR_UNSUPPORTED  # V
+    assert call(P16, 0, 4, 70000, 70000, 65537, P16, P16, None) == _native.KD_ERR_UNSUPPORTED  # K
+    assert call(P16, 0, 4, 8, 8, 9, P16, P16, None) == _native.KD_ERR_INVALID_ARG

@@ -65,14 +65,55 @@ def test_committed_traffic_record_lists_existing_sources():
             assert e["dram_bytes_per_launch"] >= e["algorithmic_bytes_per_launch"] * 0.9
 
 
-def test_gemm_tiles_description(monkeypatch):
-    monkeypatch.delenv("KD_GEMM_WIDE", raising=False)
-    monkeypatch.setenv("KD_GEMM_CTA2", "0")
-    assert bench.gemm_tiles_desc() == "128x256 per CTA"
-    monkeypatch.setenv("KD_GEMM_CTA2", "1")
-    assert "dz recompute" in bench.gemm_tiles_desc()
-    monkeypatch.setenv("KD_GEMM_WIDE", "1")
-    assert bench.gemm_tiles_desc().startswith("256x512") and "every GEMM" in bench.gemm_tiles_desc()
+def test_gemm_tiles_description():
+    from top_kl_loss_tcgen05_b300 import _native
+
+    try:
+        assert "dz recompute" in bench.gemm_tiles_desc()  # the defaults
+        _native.set_gemm_tiles(0, -1)
+        assert bench.gemm_tiles_desc() == "128x256 per CTA"
+        _native.set_gemm_tiles(1, -1)
+        assert "dz recompute" in bench.gemm_tiles_desc()
+        _native.set_gemm_tiles(1, 1)
+        assert bench.gemm_tiles_desc().startswith("256x512") and "every GEMM" in bench.gemm_tiles_desc()
+    finally:
+        _native.set_gemm_tiles(-1, -1)
+
+
+def test_default_group_is_the_library_rule():
+    """bench's description of the rows per GEMM launch follows the group the
+    library picks: the default workspace equals the explicit-group one."""
+    from top_kl_loss_tcgen05_b300 import _native
+
+    L = _native.lib()
+    for name in ("tiny", "llama3b", "gptoss20b", "long"):
+        c = bench.synth.CONFIGS[name]
+        G = bench.default_group(c["chunk"])
+        assert L.kd_fused_kl_workspace_size(c["d"], c["V"], c["K"], c["chunk"]) == \
+            L.kd_fused_kl_workspace_size_ex(c["d"], c["V"], c["K"], c["chunk"], G)
+    for chunk in (1, 100, 1024, 1500, 2048, 3000, 4096, 10000):
+        G = bench.default_group(chunk)
+        assert L.kd_fused_kl_workspace_size(256, 4096, 16, chunk) == \
+            L.kd_fused_kl_workspace_size_ex(256, 4096, 16, chunk, G)
+
+
+def test_roofline_fields_from_a_profile():
+    """The dominant kernel's achieved rate is its per-launch algorithmic flops
+    over its mean launch time, reported against the sustained and burst peaks
+    and clock-normalised."""
+    T, d, V, steps = 4096, 2880, 201088, 2
+    prof = {"grad_dH_dW": (2, 2 * 3.0), "logits_dz": (2, 2 * 1.5), "logits_fwd_lse_gather": (2, 2 * 1.4),
+            "teacher_prep": (2, 0.02)}
+    peaks = {"bf16_tflops_sustained": 1400.0, "bf16_tflops": 1800.0, "clocks_under_load": {"sm_mhz_median": 1200.0}}
+    roof, kernels, launches = bench.fused_roofline(prof, steps, T, d, V, peaks, "measured", {"sm_mhz": 1800.0},
+                                                   "long")
+    assert roof["kernel"] == "grad_dH_dW" and launches == 8
+    achieved = 4.0 * T * d * V / 3.0e-3 / 1e12
+    assert abs(roof["achieved"] - achieved) < 1e-6 * achieved
+    assert abs(roof["frac"] - achieved / 1400.0) < 1e-9
+    assert abs(roof["frac_burst"] - achieved / 1800.0) < 1e-9
+    assert abs(roof["frac_clock_normalised"] - achieved / (1400.0 * 1800.0 / 1200.0)) < 1e-9
+    assert abs(sum(k["share"] for k in kernels.values()) - 1.0) < 1e-9
 
 
 def test_max_over_ranks_single_process():

@@ -30,6 +30,16 @@ pytestmark = pytest.mark.gpu
 
 LOSS_RTOL = 1e-3
 GRAD_RTOL = 1e-2
+# Regression bound on the achieved dH / dW error (relative Frobenius). The
+# contract tolerance is GRAD_RTOL = 1e-2. What the kernels achieve is set by
+# one bf16 rounding of dz (relative rounding error ~2^-8 at most, about
+# 1.6e-3 RMS), which dH = dz W and dW = dz^T H inherit: 1.46e-3 to 1.72e-3
+# measured on B300 over the tiny, ragged and full-size cases, for the
+# recompute path and the single call alike (the norm is dominated by the
+# teacher-id entries, formed in fp32 and rounded once on both paths).
+# GRAD_ACHIEVED is about 1.5x the largest of those: an extra rounding or a
+# lost bit of the dz path fails it while the 1e-2 contract still holds.
+GRAD_ACHIEVED = 2.5e-3
 
 
 def frob(a, b):
@@ -79,6 +89,7 @@ def test_full_size_sampled_positions(cuda_dev, name):
     np.testing.assert_allclose(rows_g[S], L_o, rtol=LOSS_RTOL, atol=1e-4)
     assert abs(rows_g[S].mean() - L_o.mean()) <= LOSS_RTOL * abs(L_o.mean())
     assert frob(dH[St].cpu().numpy(), dH_o) <= GRAD_RTOL
+    assert frob(dH[St].cpu().numpy(), dH_o) <= GRAD_ACHIEVED
     # the single call (no recompute) on the same positions
     del dH
     l1, lse1, rows1, dH1, dW1 = kd.fused_kl_fwdbwd(H, W, ids, logp, chunk, want_rows=True)
@@ -88,6 +99,7 @@ def test_full_size_sampled_positions(cuda_dev, name):
     np.testing.assert_allclose(lse1.cpu().numpy()[S], lse_o, rtol=1e-5, atol=1e-5)
     np.testing.assert_allclose(r1[S], L_o, rtol=LOSS_RTOL, atol=1e-4)
     assert frob(dH1[St].cpu().numpy(), dH_o) <= GRAD_RTOL
+    assert frob(dH1[St].cpu().numpy(), dH_o) <= GRAD_ACHIEVED
 
 
 @pytest.mark.parametrize("name", ["llama3b", "gptoss20b", "long"])
@@ -113,7 +125,9 @@ def test_full_width_dW_on_truncated_run(cuda_dev, name):
         dW_o += g.T @ H64[t0:t1]
         dH_o[t0:t1] = g @ W64
     assert frob(dW.cpu().numpy(), dW_o) <= GRAD_RTOL
+    assert frob(dW.cpu().numpy(), dW_o) <= GRAD_ACHIEVED
     assert frob(dH.cpu().numpy(), dH_o) <= GRAD_RTOL
+    assert frob(dH.cpu().numpy(), dH_o) <= GRAD_ACHIEVED
 
 
 def test_teacher_cache_full_size_sampled(cuda_dev):
@@ -145,3 +159,55 @@ def test_teacher_cache_full_size_sampled(cuda_dev):
         np.testing.assert_allclose(g_lp[r], xv - lse[r], rtol=0, atol=eps)
         exact += np.array_equal(g_ids[r], ids_o[r])
     assert exact >= 0.8 * len(S)
+
+
+def test_group_one_at_llama3b_shape(cuda_dev):
+    """group = 1 (kd_kl_options.group): every GEMM launch covers one chunk of
+    1024 positions at the Llama-3.2-3B shape. Per-position results (lse, L_t,
+    dH) do not depend on the grouping at all; dW differs from the default
+    grouping by summation order only; both match the oracle. T-truncated to
+    two chunks plus a ragged tail of 37 positions."""
+    c = synth.CONFIGS["llama3b"]
+    chunk = c["chunk"]
+    Tp = 2 * chunk + 37
+    c, H, W, ids, logp = _inputs("llama3b", T=Tp)
+    ws1 = kd.fused_kl_workspace(c["d"], c["V"], c["K"], chunk, cuda_dev, group=1)
+    assert ws1.numel() < kd.fused_kl_workspace(c["d"], c["V"], c["K"], chunk, cuda_dev).numel() / 3
+    l1, lse1, r1 = kd.fused_kl_fwd(H, W, ids, logp, chunk, ws=ws1, want_rows=True, group=1)
+    dH1, dW1 = kd.fused_kl_bwd(H, W, ids, logp, lse1, chunk, 1.0 / Tp, ws=ws1, group=1)
+    l0, lse0, r0 = kd.fused_kl_fwd(H, W, ids, logp, chunk, want_rows=True)
+    dH0, dW0 = kd.fused_kl_bwd(H, W, ids, logp, lse0, chunk, 1.0 / Tp)
+    torch.cuda.synchronize()
+    assert kd.read_device_status(ws1) == 0
+    assert torch.equal(lse1, lse0) and torch.equal(r1, r0) and torch.equal(dH1, dH0)
+    assert abs(l1.item() - l0.item()) <= 1e-6 * abs(l0.item())
+    assert frob(dW1.cpu().numpy(), dW0.cpu().numpy().astype(np.float64)) <= 1e-5
+    H64 = H.float().cpu().numpy().astype(np.float64)
+    W64 = W.float().cpu().numpy().astype(np.float64)
+    idn, lpn = ids.cpu().numpy(), logp.cpu().numpy()
+    dW_o = np.zeros_like(W64)
+    dH_o = np.empty_like(H64)
+    for t0 in range(0, Tp, 256):
+        t1 = min(Tp, t0 + 256)
+        z = O.student_logits(H64[t0:t1], W64)
+        g = O.dlogits(z, idn[t0:t1], lpn[t0:t1], 1.0 / Tp)
+        dW_o += g.T @ H64[t0:t1]
+        dH_o[t0:t1] = g @ W64
+    assert frob(dW1.cpu().numpy(), dW_o) <= GRAD_RTOL
+    assert frob(dW1.cpu().numpy(), dW_o) <= GRAD_ACHIEVED
+    assert frob(dH1.cpu().numpy(), dH_o) <= GRAD_RTOL
+    assert frob(dH1.cpu().numpy(), dH_o) <= GRAD_ACHIEVED
+    # the single call with group = 1 on the same workspace: per position the
+    # same as the single call with the default group (its epilogue takes the
+    # tile maximum first, so its lse rounds differently from the forward's)
+    l2, lse2, _, dH2, dW2 = kd.fused_kl_fwdbwd(H, W, ids, logp, chunk, ws=ws1, group=1)
+    l3, lse3, _, dH3, dW3 = kd.fused_kl_fwdbwd(H, W, ids, logp, chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(lse2, lse3) and torch.equal(dH2, dH3)
+    assert frob(dW2.cpu().numpy(), dW3.cpu().numpy().astype(np.float64)) <= 1e-5
+    np.testing.assert_allclose(lse2.cpu().numpy(), lse0.cpu().numpy(), rtol=1e-6, atol=1e-6)
+    assert abs(l2.item() - l0.item()) <= 1e-5 * abs(l0.item())
+    assert frob(dW2.cpu().numpy(), dW_o) <= GRAD_RTOL
+    assert frob(dW2.cpu().numpy(), dW_o) <= GRAD_ACHIEVED
+    assert frob(dH2.cpu().numpy(), dH_o) <= GRAD_RTOL
+    assert frob(dH2.cpu().numpy(), dH_o) <= GRAD_ACHIEVED

@@ -20,19 +20,25 @@ pytestmark = pytest.mark.gpu
 
 LOSS_RTOL = 1e-3
 GRAD_RTOL = 1e-2
+# Regression bound on the achieved dH / dW error (relative Frobenius). The
+# contract tolerance is GRAD_RTOL = 1e-2. What the kernels achieve is set by
+# one bf16 rounding of dz (relative rounding error ~2^-8 at most, about
+# 1.6e-3 RMS), which dH = dz W and dW = dz^T H inherit: 1.46e-3 to 1.72e-3
+# measured on B300 over the tiny, ragged and full-size cases, for the
+# recompute path and the single call alike (the norm is dominated by the
+# teacher-id entries, formed in fp32 and rounded once on both paths).
+# GRAD_ACHIEVED is about 1.5x the largest of those: an extra rounding or a
+# lost bit of the dz path fails it while the 1e-2 contract still holds.
+GRAD_ACHIEVED = 2.5e-3
 
 
 @pytest.fixture(params=[("0", None), ("1", None), ("1", "0"), ("1", "1")],
                 ids=["cta1", "cta2", "cta2-narrow", "cta2-wide"], autouse=True)
-def gemm_tiles(request, monkeypatch):
+def gemm_tiles(request, gemm_switch):
     """Every test runs with one CTA per GEMM tile, with CTA-pair tiles at the
     per-kernel default widths, and with every pair GEMM narrow or wide."""
     cta2, wide = request.param
-    monkeypatch.setenv("KD_GEMM_CTA2", cta2)
-    if wide is None:
-        monkeypatch.delenv("KD_GEMM_WIDE", raising=False)
-    else:
-        monkeypatch.setenv("KD_GEMM_WIDE", wide)
+    gemm_switch(cta2, wide)
     return request.param
 
 
@@ -62,7 +68,9 @@ def compare(g, o):
     np.testing.assert_allclose(g["lse"], o["lse"], rtol=1e-5, atol=1e-5)
     np.testing.assert_allclose(g["rows"], o["rows"], rtol=1e-3, atol=2e-4)
     assert frob(g["dH"], o["dH"]) <= GRAD_RTOL
+    assert frob(g["dH"], o["dH"]) <= GRAD_ACHIEVED
     assert frob(g["dW"], o["dW"]) <= GRAD_RTOL
+    assert frob(g["dW"], o["dW"]) <= GRAD_ACHIEVED
 
 
 def tiny_inputs(dev):
@@ -178,4 +186,6 @@ def test_full_width_truncated_run(cuda_dev, gemm_tiles, name):
     assert abs(g["loss"] - L_o.mean()) <= LOSS_RTOL * abs(L_o.mean())
     np.testing.assert_allclose(g["rows"], L_o, rtol=LOSS_RTOL, atol=1e-4)
     assert frob(g["dW"], dW_o) <= GRAD_RTOL
+    assert frob(g["dW"], dW_o) <= GRAD_ACHIEVED
     assert frob(g["dH"], dH_o) <= GRAD_RTOL
+    assert frob(g["dH"], dH_o) <= GRAD_ACHIEVED

@@ -36,12 +36,8 @@ def frob(a, b):
 
 
 @pytest.mark.parametrize("T,d,V,K,chunk,mode,seed", _shapes())
-def test_random_shape_matches_oracle(cuda_dev, monkeypatch, T, d, V, K, chunk, mode, seed):
-    monkeypatch.setenv("KD_GEMM_CTA2", mode[0])
-    if mode[1] is None:
-        monkeypatch.delenv("KD_GEMM_WIDE", raising=False)
-    else:
-        monkeypatch.setenv("KD_GEMM_WIDE", mode[1])
+def test_random_shape_matches_oracle(cuda_dev, gemm_switch, T, d, V, K, chunk, mode, seed):
+    gemm_switch(mode[0], mode[1])
     H, W = synth.student(T, d, V, seed)
     ids, logp = synth.synthetic_cache(T, V, K, seed + 1)
     H, W, ids, logp = H.to(cuda_dev), W.to(cuda_dev), ids.to(cuda_dev), logp.to(cuda_dev)
@@ -82,13 +78,9 @@ def _variant_cases(n=12, seed=4048):
 
 
 @pytest.mark.parametrize("T,d,V,K,chunk,mode,seed,tau,masked,over,bf", _variant_cases())
-def test_random_shape_with_variants_matches_oracle(cuda_dev, monkeypatch, T, d, V, K, chunk, mode, seed, tau,
+def test_random_shape_with_variants_matches_oracle(cuda_dev, gemm_switch, T, d, V, K, chunk, mode, seed, tau,
                                                    masked, over, bf):
-    monkeypatch.setenv("KD_GEMM_CTA2", mode[0])
-    if mode[1] is None:
-        monkeypatch.delenv("KD_GEMM_WIDE", raising=False)
-    else:
-        monkeypatch.setenv("KD_GEMM_WIDE", mode[1])
+    gemm_switch(mode[0], mode[1])
     H, W = synth.student(T, d, V, seed)
     ids, logp = synth.synthetic_cache(T, V, K, seed + 1)
     mask = None

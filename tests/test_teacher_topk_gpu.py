@@ -89,14 +89,14 @@ def test_gaussian_logits_valid_against_oracle(cuda_dev):
     assert exact_rows >= 0.8 * T  # order differs only where oracle logits nearly tie
 
 
-def test_fast_and_exact_paths_agree_and_match_topk_of_the_same_logits(cuda_dev, monkeypatch):
+def test_fast_and_exact_paths_agree_and_match_topk_of_the_same_logits(cuda_dev, topk_exact):
     T, d, V, K = 200, 256, 20000, 64
     H, W = _gauss(T, d, V, 5)
     Hd, Wd = H.to(cuda_dev), W.to(cuda_dev)
     ids_f, logp_f = kd.teacher_topk_cache(Hd, Wd, K, chunk=128)
-    monkeypatch.setenv("KD_TOPK_FORCE_EXACT", "1")
+    topk_exact(True)
     ids_e, logp_e = kd.teacher_topk_cache(Hd, Wd, K, chunk=128)
-    monkeypatch.delenv("KD_TOPK_FORCE_EXACT")
+    topk_exact(False)
     torch.cuda.synchronize()
     assert torch.equal(ids_f, ids_e) and torch.equal(logp_f, logp_e)
     # the same fp32 logits from the same GEMM (pair tiles, K-major operands),

@@ -9,7 +9,7 @@ import torch
 
 import top_kl_loss_tcgen05_b300 as kd
 from oracle import kd_oracle as O
-from top_kl_loss_tcgen05_b300 import synth
+from top_kl_loss_tcgen05_b300 import _native, synth
 from topk_props import check_topk_rows
 
 pytestmark = pytest.mark.gpu
@@ -18,13 +18,12 @@ LOGP_TOL = 1e-4
 
 
 def _check(logits_dev, K, rows=None, force_exact=False):
-    if force_exact:
-        os.environ["KD_TOPK_FORCE_EXACT"] = "1"
+    _native.set_topk_force_exact(force_exact)
     try:
         ids, logp = kd.topk_cache(logits_dev, K)
         torch.cuda.synchronize()
     finally:
-        os.environ.pop("KD_TOPK_FORCE_EXACT", None)
+        _native.set_topk_force_exact(False)
     sel = slice(None) if rows is None else rows
     x = logits_dev[sel].float().cpu().numpy()
     oi, ol = O.topk_cache(x, K)

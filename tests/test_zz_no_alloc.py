@@ -40,6 +40,35 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(cuda_dev):
         assert float((logp_n - logp_w).abs().max()) <= 1e-4
 
 
+def test_noalloc_allocates_no_device_memory(cuda_dev):
+    """After the first call on the device (which looks up the array's
+    address), further calls leave the device's free memory unchanged: the
+    entry point allocates nothing, and neither does anything it calls."""
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(256, 5000, generator=g).to(torch.bfloat16).to(cuda_dev)
+    ids = torch.empty(256, 20, dtype=torch.int32, device=cuda_dev)
+    logp = torch.empty(256, 20, dtype=torch.float32, device=cuda_dev)
+    L = _native.lib()
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        rc = L.kd_topk_cache_noalloc(x.data_ptr(), _native.KD_BF16, 256, 5000, 5000, 20, ids.data_ptr(),
+                                     logp.data_ptr(), s)
+        assert rc == 0, _native.status_string(rc)
+
+    call()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    ids_w, _ = kd.topk_cache(x, 20)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids_w)
+
+
 def test_noalloc_rejects_bad_arguments(cuda_dev):
     L = _native.lib()
     assert L.kd_topk_cache_noalloc(None, 0, 4, 8, 8, 2, None, None, None) == _native.KD_ERR_INVALID_ARG

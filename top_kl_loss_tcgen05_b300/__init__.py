@@ -134,8 +134,10 @@ def teacher_topk_cache(H: torch.Tensor, W: torch.Tensor, K: int, chunk: int = 10
 # ----------------------------------------------------------------- fused KL
 
 
-def fused_kl_workspace(d: int, V: int, K: int, chunk: int, device) -> torch.Tensor:
-    n = _native.lib().kd_fused_kl_workspace_size(d, V, K, chunk)
+def fused_kl_workspace(d: int, V: int, K: int, chunk: int, device, group: int = 0) -> torch.Tensor:
+    """Workspace of the fused loss calls for this chunk and group (0 = the
+    default group rule of include/kd.h)."""
+    n = _native.lib().kd_fused_kl_workspace_size_ex(d, V, K, chunk, int(group))
     if n == 0:
         raise ValueError("invalid sizes")
     return workspace(n, device)
@@ -154,10 +156,10 @@ def _check_fused(H, W, ids, logp):
     return H.shape[0], H.shape[1], W.shape[0], ids.shape[1]
 
 
-def _options(T, dev, temperature, mask, mean_over_mask, dH_bf16):
+def _options(T, dev, temperature, mask, mean_over_mask, dH_bf16, group=0):
     """kd_kl_options for the _ex calls, or None when every option is at its
     default (the plain behaviour). Returns (struct or None, mask tensor)."""
-    if temperature == 1.0 and mask is None and not mean_over_mask and not dH_bf16:
+    if temperature == 1.0 and mask is None and not mean_over_mask and not dH_bf16 and not group:
         return None, None
     m = None
     if mask is not None:
@@ -168,7 +170,7 @@ def _options(T, dev, temperature, mask, mean_over_mask, dH_bf16):
         if m.dim() != 1 or m.shape[0] != T:
             raise ValueError("mask must be [T]")
     o = _native.KLOptions(float(temperature), m.data_ptr() if m is not None else None, 1 if mean_over_mask else 0,
-                          1 if dH_bf16 else 0)
+                          1 if dH_bf16 else 0, int(group))
     return o, m
 
 
@@ -177,17 +179,18 @@ def _optp(o):
 
 
 def fused_kl_fwd(H, W, ids, logp, chunk: int, ws=None, want_rows: bool = False, temperature: float = 1.0,
-                 mask=None, mean_over_mask: bool = False):
+                 mask=None, mean_over_mask: bool = False, group: int = 0):
     """Forward: (loss [] f32, lse [T] f32, loss_rows [T] f32 or None).
 
-    temperature, mask and mean_over_mask are the kd_kl_options of
+    temperature, mask, mean_over_mask and group are the kd_kl_options of
     include/kd.h (student softmax(z / tau), tempered teacher; positions with
-    mask == 0 excluded; the mean over T or over the included positions)."""
+    mask == 0 excluded; the mean over T or over the included positions;
+    chunks per GEMM launch, 0 = default)."""
     T, d, V, K = _check_fused(H, W, ids, logp)
     dev = H.device
     if ws is None:
-        ws = fused_kl_workspace(d, V, K, chunk, dev)
-    o, _m = _options(T, dev, temperature, mask, mean_over_mask, False)
+        ws = fused_kl_workspace(d, V, K, chunk, dev, group)
+    o, _m = _options(T, dev, temperature, mask, mean_over_mask, False, group)
     loss = torch.empty((), dtype=torch.float32, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
     rows = torch.empty(T, dtype=torch.float32, device=dev) if want_rows else None
@@ -202,7 +205,7 @@ def fused_kl_fwd(H, W, ids, logp, chunk: int, ws=None, want_rows: bool = False, 
 
 def fused_kl_bwd(H, W, ids, logp, lse, chunk: int, grad_scale: float, grad_scale_dev=None, dH=None, dW=None,
                  accumulate_dW: bool = False, ws=None, temperature: float = 1.0, mask=None,
-                 mean_over_mask: bool = False, dH_bf16: bool = False):
+                 mean_over_mask: bool = False, dH_bf16: bool = False, group: int = 0):
     """Backward: (dH [T, d] f32 (bf16 with dH_bf16), dW [V, d] f32) for
     dz = s (q - p); s = grad_scale * grad_scale_dev * 1/tau, times 1/N when
     mean_over_mask (then grad_scale is d objective / d loss)."""
@@ -210,7 +213,7 @@ def fused_kl_bwd(H, W, ids, logp, lse, chunk: int, grad_scale: float, grad_scale
     dev = H.device
     _need(lse, "lse", torch.float32, dev)
     if ws is None:
-        ws = fused_kl_workspace(d, V, K, chunk, dev)
+        ws = fused_kl_workspace(d, V, K, chunk, dev, group)
     dh_dtype = torch.bfloat16 if dH_bf16 else torch.float32
     if dH is None:
         dH = torch.empty(T, d, dtype=dh_dtype, device=dev)
@@ -220,7 +223,7 @@ def fused_kl_bwd(H, W, ids, logp, lse, chunk: int, grad_scale: float, grad_scale
     _need(dW, "dW", torch.float32, dev)
     if grad_scale_dev is not None:
         _need(grad_scale_dev, "grad_scale_dev", torch.float32, dev)
-    o, _m = _options(T, dev, temperature, mask, mean_over_mask, dH_bf16)
+    o, _m = _options(T, dev, temperature, mask, mean_over_mask, dH_bf16, group)
     check(
         "kd_fused_kl_bwd_ex",
         _native.lib().kd_fused_kl_bwd_ex(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(),
@@ -233,7 +236,7 @@ def fused_kl_bwd(H, W, ids, logp, lse, chunk: int, grad_scale: float, grad_scale
 
 def fused_kl_fwdbwd(H, W, ids, logp, chunk: int, grad_scale: float | None = None, grad_scale_dev=None, dH=None,
                     dW=None, accumulate_dW: bool = False, ws=None, want_rows: bool = False, temperature: float = 1.0,
-                    mask=None, mean_over_mask: bool = False, dH_bf16: bool = False):
+                    mask=None, mean_over_mask: bool = False, dH_bf16: bool = False, group: int = 0):
     """Forward and backward in one call, without recomputing the logits:
     (loss, lse, loss_rows or None, dH, dW). grad_scale defaults to the
     gradient of the loss itself: 1/T, or 1 with mean_over_mask (the library
@@ -241,7 +244,7 @@ def fused_kl_fwdbwd(H, W, ids, logp, chunk: int, grad_scale: float | None = None
     T, d, V, K = _check_fused(H, W, ids, logp)
     dev = H.device
     if ws is None:
-        ws = fused_kl_workspace(d, V, K, chunk, dev)
+        ws = fused_kl_workspace(d, V, K, chunk, dev, group)
     if grad_scale is None:
         grad_scale = 1.0 if (mean_over_mask and mask is not None) else 1.0 / T
     loss = torch.empty((), dtype=torch.float32, device=dev)
@@ -256,7 +259,7 @@ def fused_kl_fwdbwd(H, W, ids, logp, chunk: int, grad_scale: float | None = None
     _need(dW, "dW", torch.float32, dev)
     if grad_scale_dev is not None:
         _need(grad_scale_dev, "grad_scale_dev", torch.float32, dev)
-    o, _m = _options(T, dev, temperature, mask, mean_over_mask, dH_bf16)
+    o, _m = _options(T, dev, temperature, mask, mean_over_mask, dH_bf16, group)
     check(
         "kd_fused_kl_fwdbwd_ex",
         _native.lib().kd_fused_kl_fwdbwd_ex(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K,
@@ -272,19 +275,20 @@ class FusedKL(torch.autograd.Function):
     """loss = mean KL(p_teacher,topK || softmax(W h_t)), fused and chunked.
 
     FusedKL.apply(H, W, ids, logp, chunk, temperature=1.0, mask=None,
-    mean_over_mask=False). Forward saves only lse [T] (4 bytes per
+    mean_over_mask=False, group=0). Forward saves only lse [T] (4 bytes per
     position). Backward recomputes each chunk's logits. The upstream gradient
     goes to the kernels as a device scalar, so backward does not synchronise.
     dH comes out of the kernels in H's dtype when H is bf16.
     """
 
     @staticmethod
-    def forward(ctx, H, W, ids, logp, chunk: int, temperature: float = 1.0, mask=None, mean_over_mask: bool = False):
-        ws = fused_kl_workspace(H.shape[1], W.shape[0], ids.shape[1], chunk, H.device)
+    def forward(ctx, H, W, ids, logp, chunk: int, temperature: float = 1.0, mask=None, mean_over_mask: bool = False,
+                group: int = 0):
+        ws = fused_kl_workspace(H.shape[1], W.shape[0], ids.shape[1], chunk, H.device, group)
         loss, lse, _ = fused_kl_fwd(H, W, ids, logp, chunk, ws=ws, temperature=temperature, mask=mask,
-                                    mean_over_mask=mean_over_mask)
+                                    mean_over_mask=mean_over_mask, group=group)
         ctx.save_for_backward(H, W, ids, logp, lse)
-        ctx.chunk, ctx.ws = chunk, ws
+        ctx.chunk, ctx.ws, ctx.group = chunk, ws, group
         ctx.temperature, ctx.mask, ctx.mean_over_mask = temperature, mask, mean_over_mask
         return loss
 
@@ -295,5 +299,6 @@ class FusedKL(torch.autograd.Function):
         over_mask = bool(ctx.mean_over_mask) and ctx.mask is not None
         dH, dW = fused_kl_bwd(H, W, ids, logp, lse, ctx.chunk, 1.0 if over_mask else 1.0 / H.shape[0],
                               grad_scale_dev=g, ws=ctx.ws, temperature=ctx.temperature, mask=ctx.mask,
-                              mean_over_mask=ctx.mean_over_mask, dH_bf16=H.dtype == torch.bfloat16)
-        return dH, dW, None, None, None, None, None, None
+                              mean_over_mask=ctx.mean_over_mask, dH_bf16=H.dtype == torch.bfloat16,
+                              group=ctx.group)
+        return dH, dW, None, None, None, None, None, None, None

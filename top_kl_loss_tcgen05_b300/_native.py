@@ -35,6 +35,7 @@ SIGNATURES = {
     "kd_topk_cache": (ctypes.c_int, [_P, _I32, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
     "kd_topk_cache_noalloc": (ctypes.c_int, [_P, _I32, _I64, _I64, _I64, _I32, _P, _P, _P]),
     "kd_fused_kl_workspace_size": (_SZ, [_I64, _I64, _I32, _I64]),
+    "kd_fused_kl_workspace_size_ex": (_SZ, [_I64, _I64, _I32, _I64, _I32]),
     "kd_teacher_topk_workspace_size": (_SZ, [_I64, _I64, _I32, _I64]),
     "kd_teacher_topk_cache": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I32, _I64, _P, _P, _P, _SZ, _P]),
     "kd_fused_kl_fwd": (
@@ -70,6 +71,9 @@ SIGNATURES = {
     "kd_cache_close": (ctypes.c_int, [_P]),
     "kd_test_gemm": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32, _P, _P]),
     "kd_test_wait_timeout": (ctypes.c_int, [_I64, _P, _P]),
+    "kd_test_set_gemm_tiles": (ctypes.c_int, [_I32, _I32]),
+    "kd_test_get_gemm_tiles": (ctypes.c_int, [_P, _P]),
+    "kd_test_set_topk_force_exact": (ctypes.c_int, [_I32]),
     "kd_profile_begin": (ctypes.c_int, []),
     "kd_profile_end": (ctypes.c_int, [_P, _I32, _P]),
 }
@@ -79,7 +83,7 @@ class KLOptions(ctypes.Structure):
     """Mirror of kd_kl_options in include/kd.h."""
 
     _fields_ = [("temperature", ctypes.c_float), ("mask", ctypes.c_void_p), ("mean_over_mask", ctypes.c_int32),
-                ("dH_bf16", ctypes.c_int32)]
+                ("dH_bf16", ctypes.c_int32), ("group", ctypes.c_int32)]
 
 
 class ProfEntry(ctypes.Structure):
@@ -132,6 +136,23 @@ def profile_end() -> dict:
     n = ctypes.c_int32(0)
     check("kd_profile_end", lib().kd_profile_end(buf, 16, ctypes.byref(n)))
     return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(n.value)}
+
+
+def set_gemm_tiles(cta2: int = -1, wide: int = -1) -> None:
+    """kd_test_set_gemm_tiles (include/kd_testing.h): -1 restores a default."""
+    check("kd_test_set_gemm_tiles", lib().kd_test_set_gemm_tiles(int(cta2), int(wide)))
+
+
+def get_gemm_tiles() -> tuple:
+    """(cta2, wide) switch values of kd_test_get_gemm_tiles (-1 = default)."""
+    a, b = ctypes.c_int32(0), ctypes.c_int32(0)
+    check("kd_test_get_gemm_tiles", lib().kd_test_get_gemm_tiles(ctypes.byref(a), ctypes.byref(b)))
+    return int(a.value), int(b.value)
+
+
+def set_topk_force_exact(on: bool) -> None:
+    """kd_test_set_topk_force_exact (include/kd_testing.h)."""
+    check("kd_test_set_topk_force_exact", lib().kd_test_set_topk_force_exact(1 if on else 0))
 
 
 def check(fn: str, code: int) -> None:

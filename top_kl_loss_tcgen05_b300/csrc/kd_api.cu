@@ -18,6 +18,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -64,13 +65,19 @@ int num_sms_current() {
 }
 
 // GEMM tile shape: 1 = CTA-pair tiles (tcgen05 cta_group::2; 256 x 512 or
-// 256 x 256, see gemm_wide), 0 = one CTA per 128 x 256 tile. KD_GEMM_CTA2=0/1
-// overrides the default.
+// 256 x 256, see gemm_wide), 0 = one CTA per 128 x 256 tile.
 constexpr int kDefaultCta2 = 1;
+
+// Process-wide switches for tests and measurements (kd_testing.h). -1 keeps
+// the default. They are read on the host when a call sets up its launches;
+// nothing in the environment changes which kernels a call runs.
+std::atomic<int> g_test_cta2{-1};
+std::atomic<int> g_test_wide{-1};
+std::atomic<int> g_test_force_exact{0};
+
 int gemm_cta2() {
-  const char* e = std::getenv("KD_GEMM_CTA2");
-  if (e && (e[0] == '0' || e[0] == '1')) return e[0] - '0';
-  return kDefaultCta2;
+  const int v = g_test_cta2.load(std::memory_order_relaxed);
+  return v < 0 ? kDefaultCta2 : v;
 }
 
 // Width of the CTA-pair tiles per GEMM, chosen by measurement on B300: wide
@@ -78,19 +85,21 @@ int gemm_cta2() {
 // single call's exp-storing forward and the teacher logits; narrow (256 x 256,
 // double-buffered accumulators, so the epilogue overlaps the next tile) for
 // the dz recompute, whose epilogue costs more than the wide tile saves.
-// KD_GEMM_WIDE=0/1 forces one width everywhere (tests and measurements).
 int gemm_wide(int dflt) {
-  const char* e = std::getenv("KD_GEMM_WIDE");
-  if (e && (e[0] == '0' || e[0] == '1')) return e[0] - '0';
-  return dflt;
+  const int v = g_test_wide.load(std::memory_order_relaxed);
+  return v < 0 ? dflt : v;
 }
 
-// The backward pass groups chunks for its dH/dW GEMM, up to 4 chunks and
-// about 4096 positions per group. The dW tiles then run over a long
-// contraction (G * chunk), so their epilogue (the fp32 read-modify-write of
-// the tile, 8 V d bytes per group in all) is paid once per group, not once
-// per chunk. The workspace holds the group's dz: still O(chunk * V).
-int64_t bwd_group(int64_t chunk) {
+int topk_force_exact() { return g_test_force_exact.load(std::memory_order_relaxed) ? 1 : 0; }
+
+// Chunks per GEMM group. By default up to 4 chunks and about 4096 positions
+// per group: the dW tiles then run over a long contraction (G * chunk), so
+// their epilogue (the fp32 read-modify-write of the tile, 8 V d bytes per
+// group in all) is paid once per group, not once per chunk. A caller that
+// sizes `chunk` to bound memory passes group = 1 (kd_kl_options.group). The
+// workspace holds the group's dz: O(group * chunk * V).
+int64_t bwd_group(int64_t chunk, int64_t group) {
+  if (group > 0) return group;
   const int64_t g = 4096 / chunk;
   return g < 1 ? 1 : (g > 4 ? 4 : g);
 }
@@ -108,12 +117,12 @@ struct Layout {
   size_t ids_sorted, p_sorted, cnt, ent, zK, block_sums, part_m, part_s, hct, dz, total;
 };
 
-Layout fused_layout(int64_t d, int64_t V, int K, int64_t chunk) {
+Layout fused_layout(int64_t d, int64_t V, int K, int64_t chunk, int64_t group) {
   Layout L;
   L.Kp = (K + 3) / 4 * 4;
   L.S = ceil_div(V, kBNLogits);
   L.ldz = align_up((size_t)V, 64);
-  L.G = bwd_group(chunk);
+  L.G = bwd_group(chunk, group);
   L.ldt = align_up((size_t)(L.G * chunk), 64);
   const int64_t prow = L.G * chunk;
   size_t o = kHeader;
@@ -221,13 +230,14 @@ int cuda_status(cudaError_t e) {
 }
 
 int check_fused_args(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
-                     int64_t V, int32_t K, int64_t chunk, void* ws, size_t ws_bytes) {
+                     int64_t V, int32_t K, int64_t chunk, int64_t group, void* ws, size_t ws_bytes) {
   if (!H || !W || !ids || !logp || T <= 0 || d <= 0 || V <= 0 || K <= 0 || chunk <= 0) return KD_ERR_INVALID_ARG;
   if (K > V) return KD_ERR_INVALID_ARG;
   if (K > 4096 || V >= (int64_t(1) << 31) || d % 8 != 0 || d > (int64_t(1) << 24) || chunk > (int64_t(1) << 24))
     return KD_ERR_UNSUPPORTED;
+  if (bwd_group(chunk, group) * chunk > (int64_t(1) << 24)) return KD_ERR_UNSUPPORTED;
   if (!aligned(H, 16) || !aligned(W, 16)) return KD_ERR_UNSUPPORTED;
-  const Layout L = fused_layout(d, V, K, chunk);
+  const Layout L = fused_layout(d, V, K, chunk, group);
   if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return KD_ERR_WORKSPACE;
   return KD_OK;
 }
@@ -337,6 +347,7 @@ struct LossOpts {
   const uint8_t* mask = nullptr;
   int mean_over_mask = 0;
   int dH_bf16 = 0;
+  int64_t group = 0;  // chunks per GEMM group; 0 = the default rule (bwd_group)
 };
 
 int parse_opts(const kd_kl_options* o, LossOpts* out) {
@@ -344,12 +355,14 @@ int parse_opts(const kd_kl_options* o, LossOpts* out) {
   if (o) {
     if (!(o->temperature > 0.f) || !std::isfinite(o->temperature) || !std::isfinite(1.f / o->temperature))
       return KD_ERR_INVALID_ARG;
-    if ((o->mean_over_mask != 0 && o->mean_over_mask != 1) || (o->dH_bf16 != 0 && o->dH_bf16 != 1))
+    if ((o->mean_over_mask != 0 && o->mean_over_mask != 1) || (o->dH_bf16 != 0 && o->dH_bf16 != 1) ||
+        o->group < 0)
       return KD_ERR_INVALID_ARG;
     r.inv_tau = 1.f / o->temperature;
     r.mask = o->mask;
     r.mean_over_mask = o->mean_over_mask;
     r.dH_bf16 = o->dH_bf16;
+    r.group = o->group;
   }
   *out = r;
   return KD_OK;
@@ -451,6 +464,18 @@ cudaError_t prep_group(const int32_t* ids, const float* logp, int64_t g0, int ro
 
 }  // namespace
 
+// Argument checks of kd_topk_cache other than the workspace: null pointers,
+// sizes, dtype, alignment and the kernel's shared-memory limit.
+int topk_check_args(const void* logits, int dtype, int64_t T, int64_t V, int64_t ld, int K, const void* ids,
+                    const void* logp) {
+  if (!logits || !ids || !logp || T <= 0 || V <= 0 || K <= 0 || K > V || ld < V) return KD_ERR_INVALID_ARG;
+  if (dtype != KD_BF16 && dtype != KD_F32) return KD_ERR_INVALID_ARG;
+  if (V >= (int64_t(1) << 31) || K > 65536) return KD_ERR_UNSUPPORTED;
+  if (!aligned(logits, dtype == KD_BF16 ? 2 : 4)) return KD_ERR_UNSUPPORTED;
+  if (topk_smem_bytes(K) > 200 * 1024) return KD_ERR_UNSUPPORTED;
+  return KD_OK;
+}
+
 }  // namespace kd
 
 using namespace kd;
@@ -472,7 +497,7 @@ const char* kd_status_string(int status) {
   }
 }
 
-int kd_version(void) { return 100; }
+int kd_version(void) { return 110; }
 
 size_t kd_topk_workspace_size(int64_t T, int64_t V, int32_t K, int32_t dtype) {
   (void)T; (void)V; (void)K; (void)dtype;
@@ -481,38 +506,39 @@ size_t kd_topk_workspace_size(int64_t T, int64_t V, int32_t K, int32_t dtype) {
 
 int kd_topk_cache(const void* logits, int32_t dtype, int64_t T, int64_t V, int64_t ld, int32_t K, int32_t* ids,
                   float* logp, void* ws, size_t ws_bytes, void* stream) {
-  if (!logits || !ids || !logp || T <= 0 || V <= 0 || K <= 0 || K > V || ld < V) return KD_ERR_INVALID_ARG;
-  if (dtype != KD_BF16 && dtype != KD_F32) return KD_ERR_INVALID_ARG;
-  if (V >= (int64_t(1) << 31) || K > 65536) return KD_ERR_UNSUPPORTED;
-  if (!aligned(logits, dtype == KD_BF16 ? 2 : 4)) return KD_ERR_UNSUPPORTED;
+  const int chk = topk_check_args(logits, dtype, T, V, ld, K, ids, logp);
+  if (chk != KD_OK) return chk;
   if (!ws || !aligned(ws, 256) || ws_bytes < kHeader) return KD_ERR_WORKSPACE;
-  if (topk_smem_bytes(K) > 200 * 1024) return KD_ERR_UNSUPPORTED;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
-  const char* fe = std::getenv("KD_TOPK_FORCE_EXACT");
-  const int force = (fe && fe[0] == '1') ? 1 : 0;
+  const int force = topk_force_exact();
   ProfScope ps(K_TOPK, static_cast<cudaStream_t>(stream));
   return cuda_status(launch_topk(logits, dtype, T, V, ld, K, ids, logp, static_cast<int*>(ws), force, sms,
                                  static_cast<cudaStream_t>(stream)));
 }
 
+size_t kd_fused_kl_workspace_size_ex(int64_t d, int64_t V, int32_t K, int64_t chunk, int32_t group) {
+  if (d <= 0 || V <= 0 || K <= 0 || chunk <= 0 || group < 0) return 0;
+  return fused_layout(d, V, K, chunk, group).total;
+}
+
 size_t kd_fused_kl_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk) {
-  if (d <= 0 || V <= 0 || K <= 0 || chunk <= 0) return 0;
-  return fused_layout(d, V, K, chunk).total;
+  return kd_fused_kl_workspace_size_ex(d, V, K, chunk, 0);
 }
 
 int kd_fused_kl_fwd_ex(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
                        int64_t V, int32_t K, int64_t chunk, float* loss, float* lse, float* loss_rows,
                        const kd_kl_options* opt, void* ws, size_t ws_bytes, void* stream) {
-  int st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, ws, ws_bytes);
+  LossOpts o;
+  int st = parse_opts(opt, &o);
+  if (st != KD_OK) return st;
+  st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, o.group, ws, ws_bytes);
   if (st != KD_OK) return st;
   if (!loss || !lse) return KD_ERR_INVALID_ARG;
-  LossOpts o;
-  if ((st = parse_opts(opt, &o)) != KD_OK) return st;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const Layout L = fused_layout(d, V, K, chunk);
+  const Layout L = fused_layout(d, V, K, chunk, o.group);
   const FusedWs f = fused_ws(ws, L);
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
   // The merge kernels count finished blocks in the workspace header; the
@@ -557,16 +583,17 @@ int kd_fused_kl_bwd_ex(const void* H, const void* W, const int32_t* ids, const f
                        int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk, float grad_scale,
                        const float* grad_scale_dev, void* dH, float* dW, int32_t accumulate_dW,
                        const kd_kl_options* opt, void* ws, size_t ws_bytes, void* stream) {
-  int st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, ws, ws_bytes);
+  LossOpts o;
+  int st = parse_opts(opt, &o);
+  if (st != KD_OK) return st;
+  st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, o.group, ws, ws_bytes);
   if (st != KD_OK) return st;
   if (!lse || !dH || !dW) return KD_ERR_INVALID_ARG;
   if (!aligned(dH, 16) || !aligned(dW, 16)) return KD_ERR_UNSUPPORTED;
-  LossOpts o;
-  if ((st = parse_opts(opt, &o)) != KD_OK) return st;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const Layout L = fused_layout(d, V, K, chunk);
+  const Layout L = fused_layout(d, V, K, chunk, o.group);
   const FusedWs f = fused_ws(ws, L);
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
 
@@ -617,16 +644,17 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
                           int64_t V, int32_t K, int64_t chunk, float grad_scale, const float* grad_scale_dev,
                           float* loss, float* lse, float* loss_rows, void* dH, float* dW, int32_t accumulate_dW,
                           const kd_kl_options* opt, void* ws, size_t ws_bytes, void* stream) {
-  int st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, ws, ws_bytes);
+  LossOpts o;
+  int st = parse_opts(opt, &o);
+  if (st != KD_OK) return st;
+  st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, o.group, ws, ws_bytes);
   if (st != KD_OK) return st;
   if (!loss || !lse || !dH || !dW) return KD_ERR_INVALID_ARG;
   if (!aligned(dH, 16) || !aligned(dW, 16)) return KD_ERR_UNSUPPORTED;
-  LossOpts o;
-  if ((st = parse_opts(opt, &o)) != KD_OK) return st;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const Layout L = fused_layout(d, V, K, chunk);
+  const Layout L = fused_layout(d, V, K, chunk, o.group);
   const FusedWs f = fused_ws(ws, L);
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
   cudaError_t e = cudaMemsetAsync(f.done, 0, sizeof(unsigned), s);
@@ -707,8 +735,7 @@ int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_t d, in
   float* part_m = reinterpret_cast<float*>(w + L.part_m);
   float* part_s = reinterpret_cast<float*>(w + L.part_s);
   const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
-  const char* fe = std::getenv("KD_TOPK_FORCE_EXACT");
-  const int force = (fe && fe[0] == '1') ? 1 : 0;
+  const int force = topk_force_exact();
 
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -757,11 +784,33 @@ int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_t d, in
 int kd_read_device_status(void* ws, void* stream) {
   if (!ws) return KD_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return KD_ERR_CUDA;
+  // Read, then clear, in the order of `stream` (after the work that may have
+  // set the word), and wait for that stream alone.
   int v = 0;
-  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KD_ERR_CUDA;
-  if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return KD_ERR_CUDA;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KD_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return KD_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KD_ERR_CUDA;
   return v;
+}
+
+int kd_test_set_gemm_tiles(int32_t cta2, int32_t wide) {
+  if (cta2 < -1 || cta2 > 1 || wide < -1 || wide > 1) return KD_ERR_INVALID_ARG;
+  g_test_cta2.store(cta2, std::memory_order_relaxed);
+  g_test_wide.store(wide, std::memory_order_relaxed);
+  return KD_OK;
+}
+
+int kd_test_get_gemm_tiles(int32_t* cta2, int32_t* wide) {
+  if (!cta2 || !wide) return KD_ERR_INVALID_ARG;
+  *cta2 = g_test_cta2.load(std::memory_order_relaxed);
+  *wide = g_test_wide.load(std::memory_order_relaxed);
+  return KD_OK;
+}
+
+int kd_test_set_topk_force_exact(int32_t on) {
+  if (on != 0 && on != 1) return KD_ERR_INVALID_ARG;
+  g_test_force_exact.store(on, std::memory_order_relaxed);
+  return KD_OK;
 }
 
 int kd_test_wait_timeout(int64_t limit_ns, void* ws, void* stream) {

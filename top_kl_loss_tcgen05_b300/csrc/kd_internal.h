@@ -103,6 +103,11 @@ cudaError_t launch_finalize(const double* acc, int64_t T, const uint8_t* mask, i
 cudaError_t launch_transpose(const void* src, int rows, int cols, void* dst, int ld_dst, cudaStream_t s);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 
+// Argument checks of kd_topk_cache apart from its workspace (kd_api.cu);
+// returns a kd_status value.
+int topk_check_args(const void* logits, int dtype, int64_t T, int64_t V, int64_t ld, int K, const void* ids,
+                    const void* logp);
+
 // Top-K (kd_topk.cu).
 size_t topk_smem_bytes(int K);
 cudaError_t launch_topk(const void* logits, int dtype, int64_t T, int64_t V, int64_t ld, int K, int32_t* ids,

@@ -19,9 +19,11 @@
 #include <cstdlib>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/kd.h"
+#include "kd_internal.h"
 
 namespace {
 
@@ -30,26 +32,69 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = 4096;
 static __device__ __align__(256) unsigned char g_topk_scratch[kNoAllocScratchBytes];
 
+// Driver calls that identify the current context, so that a cached address
+// is looked up again after the device's context was torn down and recreated
+// (cudaDeviceReset reloads the module, and the array may move).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+std::once_flag g_ctx_once;
+
+void load_ctx_fns() {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+  fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(fn);
+  (void)cudaGetLastError();
+}
+
+// Id of the current context (unique for the life of the process), 0 if
+// there is none yet or it cannot be read.
+unsigned long long current_ctx_id() {
+  std::call_once(g_ctx_once, load_ctx_fns);
+  if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+  CUcontext c = nullptr;
+  if (g_ctx_get_current(&c) != CUDA_SUCCESS || !c) return 0;
+  unsigned long long id = 0;
+  if (g_ctx_get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};
 
 // Device address of g_topk_scratch on the current device. In host code the
-// name g_topk_scratch is only a host-side stand-in, so the address must come
-// from cudaGetSymbolAddress, once per device, with that device current.
+// name g_topk_scratch is only a host-side stand-in, so the address comes
+// from cudaGetSymbolAddress, with the device current: on the first call on a
+// device, and again whenever that device's context has changed since.
 int scratch_ptr(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KD_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    (void)cudaGetLastError();
+    return KD_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> g(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  const unsigned long long ctx = current_ctx_id();
+  if (!g_scratch_ptr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_topk_scratch);
     if (e != cudaSuccess || !p) {
       if (std::getenv("KD_DEBUG"))
         std::fprintf(stderr, "libkd: cudaGetSymbolAddress failed: %s\n", cudaGetErrorString(e));
+      (void)cudaGetLastError();  // do not leave the error for the caller's next CUDA call
+      g_scratch_ptr[dev] = nullptr;
       return KD_ERR_CUDA;
     }
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = current_ctx_id();  // the lookup made the context current if it was not
   }
   *out = g_scratch_ptr[dev];
   return KD_OK;
@@ -59,8 +104,10 @@ int scratch_ptr(void** out) {
 
 extern "C" int kd_topk_cache_noalloc(const void* logits, int32_t dtype, int64_t T, int64_t V, int64_t ld,
                                      int32_t K, int32_t* ids, float* logp, void* stream) {
-  if (!logits || !ids || !logp || T <= 0 || V <= 0 || K <= 0 || K > V || ld < V) return KD_ERR_INVALID_ARG;
-  if (dtype != KD_BF16 && dtype != KD_F32) return KD_ERR_INVALID_ARG;
+  // Every check of kd_topk_cache comes first, so a refused call has put
+  // nothing on the stream.
+  const int chk = kd::topk_check_args(logits, dtype, T, V, ld, K, ids, logp);
+  if (chk != KD_OK) return chk;
   const size_t need = kd_topk_workspace_size(T, V, K, dtype);
   if (need > kNoAllocScratchBytes) {
     if (std::getenv("KD_DEBUG"))
