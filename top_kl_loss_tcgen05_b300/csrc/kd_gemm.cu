@@ -124,6 +124,56 @@ __device__ __forceinline__ int lower_bound(const int* rid, int cnt, int x) {
   return lo;
 }
 
+// Runs f(v, c0) over columns [0, ncols) of a warp's TMEM rows, 32 columns
+// at a time (v: lane i holds row i's 32 fp32 values at columns c0 ...
+// c0 + 31). The load of the next 32 columns is in flight while f works on
+// the current ones (two register buffers). ncols is warp-uniform.
+template <typename F>
+__device__ __forceinline__ void tmem_sweep(uint32_t taddr, int ncols, F&& f) {
+  uint32_t va[32], vb[32];
+  const int nch = (ncols + 31) >> 5;
+  if (nch <= 0) return;
+  tmem_ld32(taddr, va);
+  tmem_wait_ld_r(va);
+  for (int c = 0; c < nch; c += 2) {
+    const bool nb = c + 1 < nch;
+    if (nb) tmem_ld32(taddr + (uint32_t)(c + 1) * 32u, vb);
+    f(va, c * 32);
+    if (nb) {
+      tmem_wait_ld_r(vb);
+      const bool na = c + 2 < nch;
+      if (na) tmem_ld32(taddr + (uint32_t)(c + 2) * 32u, va);
+      f(vb, (c + 1) * 32);
+      if (na) tmem_wait_ld_r(va);
+    }
+  }
+}
+
+// Maximum of the first lim (>= 1) of the 32 values.
+__device__ __forceinline__ float max32_lim(const uint32_t (&v)[32], int lim) {
+  if (lim >= 32) return max32(v);
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j < lim) m = fmaxf(m, u2f(v[j]));
+  return m;
+}
+
+// sum_j exp2(v_j * a + b) over the first lim of the 32 values, in four
+// independent partial sums.
+__device__ __forceinline__ float sumexp32_lim(const uint32_t (&v)[32], int lim, float a, float b) {
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  if (lim >= 32) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) s4[j & 3] += ex2(fmaf(u2f(v[j]), a, b));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < lim) s4[j & 3] += ex2(fmaf(u2f(v[j]), a, b));
+  }
+  return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+}
+
 // ------------------------------------------------------------ cluster helpers
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -459,29 +509,26 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
       // scaled by zscale = 1 / tau. With tau = 1 this is the plain logit.
       const float zscale = g.zscale, zl2 = zscale * kLog2e;
 
+      // Next teacher id of this row inside the tile (kNone if none).
+      const uint32_t hiend = (uint32_t)(n0 + nvalid);
+      auto next_id = [&]() -> uint32_t {
+        return (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
+      };
+
       if (EPI == EPI_TEACHER) {
         // Online (max, sum exp) over the tile's valid columns, 32 at a time,
         // and each 32 x 32 fp32 block stored as it is read.
         float m = -INFINITY, s = 0.f;
         const bool box_live = m0 + 32 * wq < g.rows;
-        for (int c0 = 0; c0 < nvalid; c0 += 32) {
+        tmem_sweep(taddr, nvalid, [&](uint32_t (&v)[32], int c0) {
           const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
           if (nstore >= 2) {
             if (lane == 0) bulk_wait_read<1>();
             __syncwarp();
           }
-          uint32_t v[32];
-          tmem_ld32(taddr + c0, v);
-          tmem_wait_ld();
           const int lim = nvalid - c0;
-          float cm = -INFINITY;
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) if (jj < lim) cm = fmaxf(cm, u2f(v[jj]));
-          const float mn = fmaxf(m, cm);
-          const float nb2 = -mn * kLog2e;
-          float acc_s = 0.f;
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) if (jj < lim) acc_s += ex2(fmaf(u2f(v[jj]), kLog2e, nb2));
+          const float mn = fmaxf(m, max32_lim(v, lim));
+          const float acc_s = sumexp32_lim(v, lim, kLog2e, -mn * kLog2e);
           s = s * ex2((m - mn) * kLog2e) + acc_s;
           m = mn;
 #pragma unroll
@@ -493,271 +540,172 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
           if (lane == 0) bulk_commit();
           ++nstore;
           buf ^= 1;
-        }
+        });
         if (row < g.rows && n0 < g.V) {
           g.part_m[(size_t)row * g.S + vt] = m;
           g.part_s[(size_t)row * g.S + vt] = s;
         }
-      } else if (EPI == EPI_FWDST) {
-        // Pass 1: the row's maximum over the tile's valid columns.
+      } else if (EPI == EPI_FWDST || EPI == EPI_DZ) {
+        // Pass over the tile storing bf16 values, 64 columns per TMA box
+        // (columns past V are clipped by the store):
+        //   EPI_FWDST  e = exp((z - m) / tau), m = the row's tile maximum
+        //              (a first pass), summed in fp32; and z at the teacher
+        //              ids (fp32, from the registers);
+        //   EPI_DZ     dz = s (exp(z / tau - lse) - p [j in K]); at a teacher
+        //              id the difference is formed in fp32 and rounded once.
         float m = -INFINITY;
-        for (int c0 = 0; c0 < nvalid; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(taddr + c0, v);
-          tmem_wait_ld();
-          const int lim = nvalid - c0;
-          if (lim >= 32) {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) m = fmaxf(m, u2f(v[jj]));
-          } else {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) if (jj < lim) m = fmaxf(m, u2f(v[jj]));
-          }
+        if (EPI == EPI_FWDST)
+          tmem_sweep(taddr, nvalid, [&](uint32_t (&v)[32], int c0) { m = fmaxf(m, max32_lim(v, nvalid - c0)); });
+        float sc = 0.f, nb = 0.f;
+        if (EPI == EPI_DZ) {
+          const float lse_r = (row < g.rows) ? __ldg(g.lse + row) : 0.f;
+          const bool excluded = g.mask && row < g.rows && g.mask[row] == 0;
+          sc = excluded ? 0.f : g.scale * (g.dscale ? __ldg(g.dscale) : 1.f);
+          nb = -lse_r * kLog2e;
+        } else {
+          nb = -m * zl2;
         }
-        // Pass 2: e = exp((z - m) / tau) summed in fp32 and stored as bf16,
-        // 64 columns per TMA box (columns past V are clipped by the store).
-        const float nm = -m * zl2;
-        float s = 0.f;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
         const bool box_live = m0 + 32 * wq < g.rows;
-        for (int c0 = 0; c0 < nvalid; c0 += 64) {
-          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
-          if (nstore >= 2) {
-            if (lane == 0) bulk_wait_read<1>();
+        uint32_t want = next_id();
+        uint32_t sb = 0;
+        tmem_sweep(taddr, nvalid, [&](uint32_t (&v)[32], int c0) {
+          const int h = (c0 >> 5) & 1;  // which half of the 64-column box
+          if (h == 0) {
+            sb = smem_u32(stg + buf * kStageBytesStaging);
+            if (nstore >= 2) {
+              if (lane == 0) bulk_wait_read<1>();
+              __syncwarp();
+            }
+          }
+          const int lim = nvalid - c0;
+          uint32_t pk[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            float e0 = ex2(fmaf(u2f(v[2 * jj]), zl2, nb));
+            float e1 = ex2(fmaf(u2f(v[2 * jj + 1]), zl2, nb));
+            if (EPI == EPI_DZ) {
+              e0 *= sc;
+              e1 *= sc;
+            } else if (lim >= 32) {
+              s4[jj & 3] += e0 + e1;
+            } else {
+              if (2 * jj < lim) s4[jj & 3] += e0;
+              if (2 * jj + 1 < lim) s4[jj & 3] += e1;
+            }
+            pk[jj] = pack_bf16x2(e0, e1);
+          }
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const int q = h * 4 + qq;
+            st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4), pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2],
+                         pk[4 * qq + 3]);
+          }
+          // Teacher ids in these 32 columns, from the fp32 logits in registers.
+          const uint32_t lo = (uint32_t)(n0 + c0);
+          bool mine = want < lo + 32u;
+          while (__any_sync(0xffffffffu, mine)) {
+            if (mine) {
+              const uint32_t jj = want - lo;
+              const float z = u2f(select32(v, jj));
+              if (EPI == EPI_DZ) {
+                const float q = ex2(fmaf(z, zl2, nb));
+                const float dz = sc * (q - __ldg(g.p_sorted + (size_t)row * g.Kp + k));
+                const int col = h * 32 + (int)jj;
+                const __nv_bfloat16 hb = __float2bfloat16_rn(dz);
+                st_shared_u16(sb + lane * 128 + (((col >> 3) ^ (lane & 7)) << 4) + ((col & 7) << 1),
+                              *reinterpret_cast<const uint16_t*>(&hb));
+              } else {
+                g.zK[(size_t)row * g.Kp + k] = z * zscale;
+              }
+              ++k;
+              want = next_id();
+              mine = want < lo + 32u;
+            }
+          }
+          if (h == 1 || c0 + 32 >= nvalid) {  // the 64-column box is complete
+            fence_proxy_async_smem();
             __syncwarp();
+            if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, n0 + c0 - 32 * h, m0 + 32 * wq);
+            if (lane == 0) bulk_commit();
+            ++nstore;
+            buf ^= 1;
           }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t v[32];
-            tmem_ld32(taddr + c0 + 32 * h, v);
-            tmem_wait_ld();
-            const int lim = nvalid - c0 - 32 * h;
-            uint32_t pk[16];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const float e0 = ex2(fmaf(u2f(v[2 * jj]), zl2, nm));
-              const float e1 = ex2(fmaf(u2f(v[2 * jj + 1]), zl2, nm));
-              if (2 * jj < lim) s += e0;
-              if (2 * jj + 1 < lim) s += e1;
-              pk[jj] = pack_bf16x2(e0, e1);
-            }
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              const int q = h * 4 + qq;
-              st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4), pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2],
-                           pk[4 * qq + 3]);
-            }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, n0 + c0, m0 + 32 * wq);
-          if (lane == 0) bulk_commit();
-          ++nstore;
-          buf ^= 1;
-        }
-        // Logits at the teacher ids inside the tile (fp32, from TMEM).
-        const uint32_t hiend = (uint32_t)(n0 + nvalid);
-        uint32_t want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
-        uint32_t u = __reduce_min_sync(0xffffffffu, want);
-        while (u != kNone) {
-          const uint32_t val = tmem_ld1(taddr + (u - (uint32_t)n0));
-          tmem_wait_ld();
-          if (want == u) {
-            g.zK[(size_t)row * g.Kp + k] = u2f(val) * zscale;
-            ++k;
-            want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
-          }
-          u = __reduce_min_sync(0xffffffffu, want);
-        }
-        if (row < g.rows && n0 < g.V) {
+        });
+        if (EPI == EPI_FWDST && row < g.rows && n0 < g.V) {
           g.part_m[(size_t)row * g.S + vt] = m * zscale;
-          g.part_s[(size_t)row * g.S + vt] = s;
+          g.part_s[(size_t)row * g.S + vt] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         }
       } else if (EPI == EPI_FWD) {
+        // Online (max, sum exp) per row over the tile's vocabulary slice, and
+        // the logits at the teacher ids that fall in it.
         float m = -INFINITY, s = 0.f;
-        for (int c0 = 0; c0 < nvalid; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(taddr + c0, v);
-          tmem_wait_ld();
+        uint32_t want = next_id();
+        tmem_sweep(taddr, nvalid, [&](uint32_t (&v)[32], int c0) {
           const int lim = nvalid - c0;
-          float cm = -INFINITY;
-          if (lim >= 32) {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) cm = fmaxf(cm, u2f(v[jj]));
-          } else {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) if (jj < lim) cm = fmaxf(cm, u2f(v[jj]));
-          }
-          const float mn = fmaxf(m, cm);
-          const float nb2 = -mn * zl2;
-          float acc_s = 0.f;
-          if (lim >= 32) {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) acc_s += ex2(fmaf(u2f(v[jj]), zl2, nb2));
-          } else {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) if (jj < lim) acc_s += ex2(fmaf(u2f(v[jj]), zl2, nb2));
-          }
+          const float mn = fmaxf(m, max32_lim(v, lim));
+          const float acc_s = sumexp32_lim(v, lim, zl2, -mn * zl2);
           s = s * ex2((m - mn) * zl2) + acc_s;
           m = mn;
-        }
-        // Logits at the teacher ids inside [n0, n0 + nvalid): one TMEM column
-        // per distinct id in the warp's 32 rows.
-        const uint32_t hiend = (uint32_t)(n0 + nvalid);
-        uint32_t want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
-        uint32_t u = __reduce_min_sync(0xffffffffu, want);
-        while (u != kNone) {
-          const uint32_t val = tmem_ld1(taddr + (u - (uint32_t)n0));
-          tmem_wait_ld();
-          if (want == u) {
-            g.zK[(size_t)row * g.Kp + k] = u2f(val) * zscale;
-            ++k;
-            want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
+          const uint32_t lo = (uint32_t)(n0 + c0);
+          bool mine = want < lo + 32u;
+          while (__any_sync(0xffffffffu, mine)) {
+            if (mine) {
+              g.zK[(size_t)row * g.Kp + k] = u2f(select32(v, want - lo)) * zscale;
+              ++k;
+              want = next_id();
+              mine = want < lo + 32u;
+            }
           }
-          u = __reduce_min_sync(0xffffffffu, want);
-        }
+        });
         if (row < g.rows && n0 < g.V) {
           g.part_m[(size_t)row * g.S + vt] = m * zscale;
           g.part_s[(size_t)row * g.S + vt] = s;
         }
-      } else if (EPI == EPI_DZ) {
-        const float lse_r = (row < g.rows) ? __ldg(g.lse + row) : 0.f;
-        const bool excluded = g.mask && row < g.rows && g.mask[row] == 0;
-        const float sc = excluded ? 0.f : g.scale * (g.dscale ? __ldg(g.dscale) : 1.f);
-        const float nl = -lse_r * kLog2e;
-        const bool box_live = m0 + 32 * wq < g.rows;
-        for (int c0 = 0; c0 < nvalid; c0 += 64) {
-          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
-          if (nstore >= 2) {
-            if (lane == 0) bulk_wait_read<1>();
-            __syncwarp();
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t v[32];
-            tmem_ld32(taddr + c0 + 32 * h, v);
-            tmem_wait_ld();
-            uint32_t pk[16];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const float e0 = ex2(fmaf(u2f(v[2 * jj]), zl2, nl)) * sc;
-              const float e1 = ex2(fmaf(u2f(v[2 * jj + 1]), zl2, nl)) * sc;
-              pk[jj] = pack_bf16x2(e0, e1);
-            }
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              const int q = h * 4 + qq;
-              st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4), pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2],
-                           pk[4 * qq + 3]);
-            }
-          }
-          // Teacher ids in this 64-column group: dz = s (q - p) in fp32.
-          const uint32_t hiend = (uint32_t)(n0 + min(c0 + 64, nvalid));
-          uint32_t want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
-          uint32_t u = __reduce_min_sync(0xffffffffu, want);
-          while (u != kNone) {
-            const uint32_t val = tmem_ld1(taddr + (u - (uint32_t)n0));
-            tmem_wait_ld();
-            if (want == u) {
-              const float q = ex2(fmaf(u2f(val), zl2, nl));
-              const float dz = sc * (q - __ldg(g.p_sorted + (size_t)row * g.Kp + k));
-              const int jj = (int)(u - (uint32_t)n0) - c0;
-              const __nv_bfloat16 hb = __float2bfloat16_rn(dz);
-              st_shared_u16(sb + lane * 128 + (((jj >> 3) ^ (lane & 7)) << 4) + ((jj & 7) << 1),
-                            *reinterpret_cast<const uint16_t*>(&hb));
-              ++k;
-              want = (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
-            }
-            u = __reduce_min_sync(0xffffffffu, want);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, n0 + c0, m0 + 32 * wq);
-          if (lane == 0) bulk_commit();
-          ++nstore;
-          buf ^= 1;
-        }
-      } else if (P.c_trans && P.out_bf16) {
-        // C^T in bf16: each warp stages 32 C rows x 32 C columns as 64-byte
-        // rows (2 bytes per lane per row; a warp's 32 lanes fill one row, so
-        // the stores are conflict-free) and stores them with one
-        // non-swizzled TMA box.
-        const CUtensorMap* mC = &g.tmC[tl.prob];
-        const bool box_live = m0 + 32 * wq < P.M;
-        for (int c0 = 0; c0 < BN && n0 + c0 < P.N; c0 += 32) {
-          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
-          if (nstore >= 2) {
-            if (lane == 0) bulk_wait_read<1>();
-            __syncwarp();
-          }
-          uint32_t v[32];
-          tmem_ld32(taddr + c0, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int r = 0; r < 32; ++r) {
-            const __nv_bfloat16 h = __float2bfloat16_rn(u2f(v[r]));
-            st_shared_u16(sb + r * 64 + lane * 2, *reinterpret_cast<const uint16_t*>(&h));
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && box_live) tma_store_2d(mC, sb, m0 + 32 * wq, n0 + c0);
-          if (lane == 0) bulk_commit();
-          ++nstore;
-          buf ^= 1;
-        }
-      } else if (P.c_trans) {
-        // C is stored transposed: TMEM lane = column of C, TMEM column = row
-        // of C. Each warp stages a 32 x 32 block as [C row][C column] with
-        // one 4-byte store per element (conflict-free under the 128-byte
-        // swizzle) and stores it with one TMA box.
-        const CUtensorMap* mC = &g.tmC[tl.prob];
-        const bool box_live = m0 + 32 * wq < P.M;
-        for (int c0 = 0; c0 < BN && n0 + c0 < P.N; c0 += 32) {
-          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
-          if (nstore >= 2) {
-            if (lane == 0) bulk_wait_read<1>();
-            __syncwarp();
-          }
-          uint32_t v[32];
-          tmem_ld32(taddr + c0, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int r = 0; r < 32; ++r)
-            st_shared_b32(sb + r * 128 + ((((uint32_t)lane >> 2) ^ (uint32_t)(r & 7)) << 4) + ((lane & 3) << 2), v[r]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && box_live) {
-            if (P.reduce_add) tma_reduce_add_2d(mC, sb, m0 + 32 * wq, n0 + c0);
-            else tma_store_2d(mC, sb, m0 + 32 * wq, n0 + c0);
-          }
-          if (lane == 0) bulk_commit();
-          ++nstore;
-          buf ^= 1;
-        }
       } else {
+        // EPI_GRAD: the fp32 tile, 32 columns per TMA box, stored or
+        // reduce-added into C, or written as C^T (TMEM lanes are then C's
+        // columns): fp32, or bf16 in 64-byte rows without swizzle.
         const CUtensorMap* mC = &g.tmC[tl.prob];
         const bool box_live = m0 + 32 * wq < P.M;
-        for (int c0 = 0; c0 < BN && n0 + c0 < P.N; c0 += 32) {
+        const int ncols = min(BN, P.N - n0);
+        tmem_sweep(taddr, ncols, [&](uint32_t (&v)[32], int c0) {
           const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
           if (nstore >= 2) {
             if (lane == 0) bulk_wait_read<1>();
             __syncwarp();
           }
-          uint32_t v[32];
-          tmem_ld32(taddr + c0, v);
-          tmem_wait_ld();
+          if (P.c_trans && P.out_bf16) {
+            // a warp's 32 lanes fill one 64-byte row: conflict-free
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int r = 0; r < 32; ++r) {
+              const __nv_bfloat16 hv = __float2bfloat16_rn(u2f(v[r]));
+              st_shared_u16(sb + r * 64 + lane * 2, *reinterpret_cast<const uint16_t*>(&hv));
+            }
+          } else if (P.c_trans) {
+            // [C row][C column], one 4-byte store per element, conflict-free
+            // under the 128-byte swizzle
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+              st_shared_b32(sb + r * 128 + ((((uint32_t)lane >> 2) ^ (uint32_t)(r & 7)) << 4) + ((lane & 3) << 2), v[r]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && box_live) {
-            if (P.reduce_add) tma_reduce_add_2d(mC, sb, n0 + c0, m0 + 32 * wq);
+            if (P.c_trans && P.out_bf16) tma_store_2d(mC, sb, m0 + 32 * wq, n0 + c0);
+            else if (P.c_trans && P.reduce_add) tma_reduce_add_2d(mC, sb, m0 + 32 * wq, n0 + c0);
+            else if (P.c_trans) tma_store_2d(mC, sb, m0 + 32 * wq, n0 + c0);
+            else if (P.reduce_add) tma_reduce_add_2d(mC, sb, n0 + c0, m0 + 32 * wq);
             else tma_store_2d(mC, sb, n0 + c0, m0 + 32 * wq);
           }
           if (lane == 0) bulk_commit();
           ++nstore;
           buf ^= 1;
-        }
+        });
       }
       // Release the accumulator (C2: the even CTA's barrier counts both CTAs).
       tc_fence_before();

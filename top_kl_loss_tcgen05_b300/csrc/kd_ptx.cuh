@@ -197,6 +197,49 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// Waits for this thread's outstanding tcgen05.ld, like tmem_wait_ld, and
+// ties the 32 registers of an earlier tmem_ld32 to the wait, so that no use
+// of them can be scheduled before it (the load is asynchronous: the
+// registers are valid only after the wait).
+__device__ __forceinline__ void tmem_wait_ld_r(uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+        "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+        "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]),
+        "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+        "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
+
+// r[i] for a per-lane index i in [0, 32), by a select tree over the
+// registers (no local-memory indexing).
+__device__ __forceinline__ uint32_t select32(const uint32_t (&r)[32], uint32_t i) {
+  uint32_t t16[16], t8[8], t4[4], t2[2];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t16[j] = (i & 16u) ? r[j + 16] : r[j];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) t8[j] = (i & 8u) ? t16[j + 8] : t16[j];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) t4[j] = (i & 4u) ? t8[j + 4] : t8[j];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) t2[j] = (i & 2u) ? t4[j + 2] : t4[j];
+  return (i & 1u) ? t2[1] : t2[0];
+}
+
+// Maximum of the 32 values as fp32, as a 5-level tree (no 32-deep chain).
+__device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
+  float t[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t[j] = fmaxf(__uint_as_float(r[j]), __uint_as_float(r[j + 16]));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+  return t[0];
+}
+
 // One column: lane i gets TMEM (taddr.lane + i, taddr.col).
 __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
   uint32_t v;
