@@ -86,8 +86,7 @@ def gemm_tiles_desc() -> str:
         return "128x256 per CTA"
     if wide in (0, 1):
         return "%s per CTA pair (tcgen05 cta_group::2), every GEMM" % ("256x512" if wide == 1 else "256x256")
-    return ("256x512 per CTA pair for every GEMM but the dz recompute, which uses 256x256 "
-            "(tcgen05 cta_group::2)")
+    return "256x512 per CTA pair (tcgen05 cta_group::2), every GEMM"
 
 
 def default_group(chunk: int) -> int:
