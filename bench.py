@@ -185,9 +185,11 @@ def blas_threads() -> int:
 # ----------------------------------------------------------------------------- workload
 
 
-def make_workload(name: str, dev: torch.device):
+def make_workload(name: str, dev: torch.device, rows: int | None = None):
     c = synth.CONFIGS[name]
     T, d, V, K, chunk, seed = c["T"], c["d"], c["V"], c["K"], c["chunk"], c["seed"]
+    if rows:
+        T = min(T, int(rows))
     H, W = synth.student(T, d, V, seed, device=dev)
     # teacher cache: perturbed-W teacher logits (fp32, chunk by chunk) -> kd_topk_cache
     Wt = synth.teacher_weight(W, seed)
@@ -206,9 +208,13 @@ def make_workload(name: str, dev: torch.device):
     return dict(T=T, d=d, V=V, K=K, chunk=chunk, H=H, W=W, ids=ids, logp=logp)
 
 
-def describe(name: str) -> str:
+def describe(name: str, rows: int | None = None) -> str:
     c = synth.CONFIGS[name]
-    return "%s: T=%d d=%d V=%d K=%d chunk=%d" % (name, c["T"], c["d"], c["V"], c["K"], c["chunk"])
+    T = min(c["T"], int(rows)) if rows else c["T"]
+    out = "%s: T=%d d=%d V=%d K=%d chunk=%d" % (name, T, c["d"], c["V"], c["K"], c["chunk"])
+    if T != c["T"]:
+        out += " (first %d of its %d positions)" % (T, c["T"])
+    return out
 
 
 # ----------------------------------------------------------------------------- oracle (cpu baseline)
@@ -453,10 +459,11 @@ class FusedRun:
     """Device buffers and the fused-loss step (kd_fused_kl_fwd then
     kd_fused_kl_bwd, through the C ABI) of one workload."""
 
-    def __init__(self, name, dev):
+    def __init__(self, name, dev, rows=None):
         self.name = name
+        self.rows = rows
         self.dev = dev
-        wl = make_workload(name, dev)
+        wl = make_workload(name, dev, rows)
         self.wl = wl
         self.T, self.d, self.V, self.K, self.chunk = wl["T"], wl["d"], wl["V"], wl["K"], wl["chunk"]
         self.H, self.W, self.ids, self.logp = wl["H"], wl["W"], wl["ids"], wl["logp"]
@@ -536,7 +543,7 @@ class FusedRun:
 
 def config_desc(run: FusedRun) -> dict:
     G = default_group(run.chunk)
-    return {"workload": describe(run.name), "group": G, "rows_per_gemm_launch": G * run.chunk,
+    return {"workload": describe(run.name, run.rows), "group": G, "rows_per_gemm_launch": G * run.chunk,
             "group_note": "each GEMM launch covers a group of G chunks (the library's default group rule); the "
                           "workspace holds one group's bf16 dz"}
 
@@ -580,6 +587,10 @@ def main():
     ap.add_argument("--no-teacher", action="store_true", help="skip timing the teacher-side cache")
     ap.add_argument("--no-others", action="store_true", help="skip timing the other loss workloads")
     ap.add_argument("--topk-rows", type=int, default=None, help="rows of the top-K workload (default 8192)")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="positions of the loss workload (default: all of it). A truncated run keeps d, V, K and the "
+                         "chunk, so each GEMM launch does the same work as in the full run: for small profiling "
+                         "captures, not for bench lines")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup(args)
@@ -590,7 +601,7 @@ def main():
     peaks, peaks_src = load_peaks()
     _native.load()
 
-    run = FusedRun(args.workload, dev)
+    run = FusedRun(args.workload, dev, args.rows)
     T, d, V, K, chunk = run.T, run.d, run.V, run.K, run.chunk
     H, W, ids, logp = run.H, run.W, run.ids, run.logp
     peak_gib = run.peak_step()

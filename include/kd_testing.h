@@ -25,6 +25,9 @@ extern "C" {
  *                cta_group::2); needs b_mn == 0 (else KD_ERR_UNSUPPORTED).
  *   flags bit 3: with bit 2, wide pair tiles (256 x 512, one 512-column
  *                accumulator, eight epilogue warps).
+ *   flags bit 4: with bits 2 and 3, 256 x 480 tiles (two N = 240 MMAs; the
+ *                backward's dW uses them when d is a multiple of 480 but not
+ *                of 512); C not transposed (else KD_ERR_UNSUPPORTED).
  * Requires K, and M or N for MN-major operands, to be multiples of 8, and
  * C's row length a multiple of 4. `ws` (>= 256 bytes, device) holds the
  * status word and the tile counter. Returns a kd_status value. */

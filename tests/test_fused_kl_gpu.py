@@ -126,6 +126,7 @@ def _cache(T, V, K, seed, dev, edge=True):
     (129, 72, 4099, 33, 64),      # K-dim smaller than one 128-wide block in dW
     (64, 520, 257, 5, 64),        # V = one full logits tile + 1
     (77, 8, 31, 3, 16),           # tiny d and V
+    (300, 960, 1000, 7, 128),     # d a multiple of 480, not of 512: dW in 480-wide tiles
 ])
 def test_ragged_shapes_match_oracle(cuda_dev, T, d, V, K, chunk):
     H, W = synth.student(T, d, V, seed=T * 7 + d)

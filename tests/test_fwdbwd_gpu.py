@@ -109,6 +109,7 @@ def test_matches_separate_calls_and_is_reproducible(cuda_dev):
     (64, 520, 257, 5, 64),        # V = one full vocabulary tile + 1
     (77, 8, 31, 3, 16),           # tiny d and V
     (600, 128, 3000, 16, 2048),   # one group shorter than the chunk
+    (300, 960, 1000, 7, 128),     # d a multiple of 480, not of 512: dW in 480-wide tiles
 ])
 def test_ragged_shapes_match_oracle(cuda_dev, T, d, V, K, chunk):
     H, W = synth.student(T, d, V, seed=T * 7 + d)

@@ -12,7 +12,7 @@ from top_kl_loss_tcgen05_b300 import _native, workspace
 pytestmark = pytest.mark.gpu
 
 
-def _run(M, N, K, a_mn, b_mn, reduce_add=False, seed=0, c_trans=False, pair=False, wide=False):
+def _run(M, N, K, a_mn, b_mn, reduce_add=False, seed=0, c_trans=False, pair=False, wide=False, n240=False):
     dev = torch.device("cuda:0")
     g = torch.Generator(device=dev).manual_seed(seed)
     A = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
@@ -23,7 +23,8 @@ def _run(M, N, K, a_mn, b_mn, reduce_add=False, seed=0, c_trans=False, pair=Fals
     C0 = torch.randn(*shape, generator=g, device=dev) if reduce_add else torch.full(shape, float("nan"), device=dev)
     C = C0.clone()
     ws = workspace(256, dev)
-    flags = (1 if reduce_add else 0) | (2 if c_trans else 0) | (4 if pair else 0) | (8 if wide else 0)
+    flags = (1 if reduce_add else 0) | (2 if c_trans else 0) | (4 if pair else 0) | (8 if wide else 0) | \
+        (16 if n240 else 0)
     rc = _native.lib().kd_test_gemm(Ain.data_ptr(), Bin.data_ptr(), C.data_ptr(), M, N, K, a_mn, b_mn,
                                     flags, ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert rc == 0, _native.status_string(rc)
@@ -93,6 +94,30 @@ def test_pair_tiles_transposed_store(cuda_dev, a_mn, wide):
     _run(264, 1000, 520, a_mn, 0, seed=5, c_trans=True, pair=True, wide=wide)
     _run(3072, 1024, 4096, a_mn, 0, seed=6, c_trans=True, pair=True, wide=wide)
     _run(136, 520, 64, 1, 0, reduce_add=True, seed=7, c_trans=True, pair=True, wide=wide)
+
+
+@pytest.mark.parametrize("a_mn", [0, 1])
+def test_480_wide_tiles(cuda_dev, a_mn):
+    """256 x 480 pair tiles (two N = 240 MMAs, the dW tile at d = 2880): exact
+    and ragged N, the 16-column tail box of each half, stores and reduce-adds
+    that must not touch the neighbouring tile's columns."""
+    _run(256, 480, 128, a_mn, 0, pair=True, wide=True, n240=True)
+    _run(512, 2880, 256, a_mn, 0, seed=11, pair=True, wide=True, n240=True)              # the dW width
+    _run(1000, 2880, 200, a_mn, 0, seed=12, reduce_add=True, pair=True, wide=True, n240=True)
+    _run(296, 1000, 72, a_mn, 0, seed=13, pair=True, wide=True, n240=True)               # ragged N: 480 + 480 + 40
+    _run(136, 232, 64, a_mn, 0, seed=14, pair=True, wide=True, n240=True)                # one half, ends mid-tail
+    _run(256 * 20, 480 * 6, 320, a_mn, 0, seed=15, reduce_add=True, pair=True, wide=True, n240=True)
+
+
+def test_480_wide_tiles_refused_outside_wide_pairs(cuda_dev):
+    dev = torch.device("cuda:0")
+    A = torch.zeros(64, 64, dtype=torch.bfloat16, device=dev)
+    C = torch.zeros(64, 64, device=dev)
+    ws = workspace(256, dev)
+    for flags in (16, 16 | 4, 16 | 4 | 8 | 2):
+        rc = _native.lib().kd_test_gemm(A.data_ptr(), A.data_ptr(), C.data_ptr(), 64, 64, 64, 0, 0, flags,
+                                        ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert rc == 2  # KD_ERR_UNSUPPORTED, nothing launched
 
 
 def test_pair_tiles_reject_n_major_b(cuda_dev):

@@ -282,6 +282,11 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
                __nv_bfloat16* hct, void* dH, int dH_bf16, int64_t g0, int grows, int64_t d, int64_t V,
                int reduce_add, int sms, cudaStream_t s) {
   const int TR = gemm_tile_rows(ag.cta2), BR = gemm_b_box_rows(ag.cta2);
+  // dW's N runs over d. With wide pair tiles and d a multiple of 480 but not
+  // of 512 (d = 2880 at the GPT-OSS shapes), 480-wide tiles (two N = 240
+  // MMAs) cover d exactly; 512-wide ones would spend 6.25% of dW's MMAs on
+  // padding.
+  const bool dw480 = ag.cta2 && ag.wide && d % 512 != 0 && d % 480 == 0;
   cudaError_t e;
   {
     ProfScope ps(K_TRANSPOSE, s);
@@ -300,7 +305,7 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
       encode_map_2d(&ag.tmA[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
                     (uint64_t)L.ldz * 2, 64, 64) != cudaSuccess ||
       encode_map_2d(&ag.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, hct, (uint64_t)grows, (uint64_t)d,
-                    (uint64_t)L.ldt * 2, kBK, BR) != cudaSuccess)
+                    (uint64_t)L.ldt * 2, kBK, dw480 ? 120 : BR) != cudaSuccess)
     return KD_ERR_UNSUPPORTED;
   Problem& P0 = ag.pr[0];
   P0.m_blocks = (int)ceil_div(d, TR);
@@ -308,9 +313,11 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
   P0.k_blocks = (int)ceil_div(V, kBK);
   P0.a_mn = 1; P0.b_mn = 0; P0.M = (int)d; P0.N = grows;
   P0.tile_begin = 0; P0.n_fastest = 0; P0.reduce_add = 0; P0.c_trans = 1; P0.out_bf16 = dH_bf16;
+  P0.bnh = 256;
   Problem& P1 = ag.pr[1];
   P1.m_blocks = (int)ceil_div(V, TR);
-  P1.n_blocks = (int)ceil_div(d, gemm_tile_cols(ag.cta2, ag.wide));
+  P1.n_blocks = (int)(dw480 ? d / 480 : ceil_div(d, gemm_tile_cols(ag.cta2, ag.wide)));
+  P1.bnh = dw480 ? 240 : 256;
   P1.k_blocks = (int)ceil_div(grows, kBK);
   P1.a_mn = 1; P1.b_mn = 0; P1.M = (int)V; P1.N = (int)d;
   P1.tile_begin = P0.m_blocks * P0.n_blocks; P1.n_fastest = 1;
@@ -336,7 +343,9 @@ int grad_setup(GemmArgs& ag, const void* W, float* dW, int64_t d, int64_t V, int
   if (encode_map_2d(&ag.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, 64,
                     64) != cudaSuccess ||
       encode_map_2d(&ag.tmC[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, (uint64_t)d, (uint64_t)V, (uint64_t)d * 4, 32,
-                    32) != cudaSuccess)
+                    32) != cudaSuccess ||
+      encode_map_2d_plain(&ag.tmCt[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, (uint64_t)d, (uint64_t)V,
+                          (uint64_t)d * 4, 16, 32) != cudaSuccess)
     return KD_ERR_UNSUPPORTED;
   return KD_OK;
 }
@@ -822,9 +831,11 @@ int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, i
                  int32_t b_mn, int32_t flags, void* ws, void* stream) {
   if (!A || !B || !C || !ws || M <= 0 || N <= 0 || K <= 0) return KD_ERR_INVALID_ARG;
   const int reduce_add = flags & 1, c_trans = (flags >> 1) & 1, cta2 = (flags >> 2) & 1, wide = (flags >> 3) & 1;
+  const int n240 = (flags >> 4) & 1;  // 480-wide pair tiles (two N = 240 MMAs)
   const int64_t ldc = c_trans ? M : N;  // C is [M, N], or [N, M] when stored transposed
   if (K % 8 || (a_mn && M % 8) || (b_mn && N % 8) || ldc % 4) return KD_ERR_UNSUPPORTED;
   if (cta2 && b_mn) return KD_ERR_UNSUPPORTED;  // the pair tiles read a K-major B only
+  if (n240 && (!cta2 || !wide || c_trans)) return KD_ERR_UNSUPPORTED;  // wide pair tiles, plain C only
   if (M >= (1 << 30) || N >= (1 << 30) || K >= (1 << 30)) return KD_ERR_UNSUPPORTED;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
@@ -834,17 +845,20 @@ int kd_test_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, i
                         : encode_map_2d(&a.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, kBK, kBM);
   cudaError_t e2 = b_mn ? encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, N * 2, 64, 64)
                         : encode_map_2d(&a.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, K * 2, kBK,
-                                        gemm_b_box_rows(cta2));
+                                        n240 ? 120 : gemm_b_box_rows(cta2));
   cudaError_t e3 = c_trans ? encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, M, N, M * 4, 32, 32)
                            : encode_map_2d(&a.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, 32);
   if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return KD_ERR_UNSUPPORTED;
+  if (n240 && encode_map_2d_plain(&a.tmCt[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 16, 32) != cudaSuccess)
+    return KD_ERR_UNSUPPORTED;
   a.cta2 = cta2;
   a.wide = wide;
   a.zscale = 1.f;
   Problem& P = a.pr[0];
   P.m_blocks = (int)ceil_div(M, gemm_tile_rows(cta2));
-  P.n_blocks = (int)ceil_div(N, gemm_tile_cols(cta2, wide));
+  P.n_blocks = (int)ceil_div(N, n240 ? 480 : gemm_tile_cols(cta2, wide));
   P.k_blocks = (int)ceil_div(K, kBK);
+  P.bnh = n240 ? 240 : 256;
   P.a_mn = a_mn ? 1 : 0; P.b_mn = b_mn ? 1 : 0;
   P.M = (int)M; P.N = (int)N;
   P.tile_begin = 0; P.n_fastest = 0; P.reduce_add = reduce_add; P.c_trans = c_trans;

@@ -294,6 +294,7 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
       tma_prefetch_desc(&g.tmA[p]);
       tma_prefetch_desc(&g.tmB[p]);
       if (EPI != EPI_FWD) tma_prefetch_desc(&g.tmC[p]);
+      if (EPI == EPI_GRAD && g.pr[p].bnh == 240) tma_prefetch_desc(&g.tmCt[p]);
     }
   }
   if (warp == 1) tmem_alloc_x<C2>(tmem_slot);
@@ -340,16 +341,21 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
         const CUtensorMap* mA = &g.tmA[tl.prob];
         const CUtensorMap* mB = &g.tmB[tl.prob];
         const int am = tl.mb * C::TM + (int)rank * kBM;  // this CTA's first A row (M)
-        // this CTA's first B row (N); wide pair tiles load a second box 256
+        // N of one MMA: wide pair tiles run two of them, bnh columns apart
+        // (each CTA loads bnh / 2 B rows for each); 256 otherwise
+        const int bnh = (C::W && P.bnh) ? P.bnh : BN;
+        // this CTA's first B row (N); wide pair tiles load a second box bnh
         // rows further
-        const int bn = C2 ? tl.nb * C::TN + (int)rank * 128 : tl.nb * C::TN;
+        const int bn = C2 ? (C::W ? tl.nb * 2 * bnh + (int)rank * (bnh / 2) : tl.nb * C::TN + (int)rank * 128)
+                          : tl.nb * C::TN;
+        const uint32_t tx = C::W ? 2u * (C::A_BYTES + 2u * (uint32_t)(bnh / 2) * 128u) : C::TX;
         for (int kb = 0; kb < P.k_blocks; ++kb) {
           if (!mbar_wait<C2>(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t sA = smem_u32(smem + stage * C::STAGE);
           const uint32_t sB = sA + C::A_BYTES;
           if (C2) {
             const uint32_t fb = full0_c + (uint32_t)stage * 8u;
-            if (leader) mbar_arrive_expect_tx(&full[stage], C::TX);
+            if (leader) mbar_arrive_expect_tx(&full[stage], tx);
             if (!P.a_mn) {
               tma_load_2d_pair(sA, mA, fb, kb * kBK, am);
             } else {
@@ -357,7 +363,7 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
               for (int q = 0; q < kBM / 64; ++q) tma_load_2d_pair(sA + q * 8192, mA, fb, am + q * 64, kb * kBK);
             }
             tma_load_2d_pair(sB, mB, fb, kb * kBK, bn);  // (wide: N half 0)
-            if (C::W) tma_load_2d_pair(sB + 16384, mB, fb, kb * kBK, bn + 256);  // N half 1
+            if (C::W) tma_load_2d_pair(sB + 16384, mB, fb, kb * kBK, bn + bnh);  // N half 1
           } else {
             mbar_arrive_expect_tx(&full[stage], C::TX);
             if (!P.a_mn) {
@@ -420,7 +426,7 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);  // wide: acc = 0, columns [0, 512)
         const int b_mn = C2 ? 0 : P.b_mn;
-        const uint32_t idesc = idesc_bf16_f32(C::TM, BN, P.a_mn, b_mn);
+        const uint32_t idesc = idesc_bf16_f32(C::TM, (C::W && P.bnh) ? P.bnh : BN, P.a_mn, b_mn);
         for (int kb = 0; kb < P.k_blocks; ++kb) {
           if (!mbar_wait<C2>(&full[stage], phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -483,7 +489,8 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
       const int m0 = tl.mb * C::TM + (int)rank * kBM;  // first tile row held in this CTA's TMEM
       const int row = m0 + 32 * wq + lane;
       const int vt = tl.nb * (C::TN / BN) + hc;  // the 256-column block (vocabulary tile) of this warp
-      const int n0 = vt * BN;
+      const int bnh = (C::W && P.bnh) ? P.bnh : BN;  // columns of this warp's half (256, or 240)
+      const int n0 = vt * bnh;
 
       // Teacher-id cursor of this row for the tile's vocabulary slice.
       int cnt = 0, k = 0;
@@ -667,12 +674,29 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
         // columns): fp32, or bf16 in 64-byte rows without swizzle.
         const CUtensorMap* mC = &g.tmC[tl.prob];
         const bool box_live = m0 + 32 * wq < P.M;
-        const int ncols = min(BN, P.N - n0);
+        const int ncols = min(bnh, P.N - n0);
         tmem_sweep(taddr, ncols, [&](uint32_t (&v)[32], int c0) {
           const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
           if (nstore >= 2) {
             if (lane == 0) bulk_wait_read<1>();
             __syncwarp();
+          }
+          if (c0 + 32 > bnh) {
+            // the last 16 columns of a 240-wide half (plain fp32 C): a 16-column
+            // box, so nothing is stored into the neighbouring tile's columns
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(sb + lane * 64 + q * 16, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && box_live) {
+              if (P.reduce_add) tma_reduce_add_2d(&g.tmCt[tl.prob], sb, n0 + c0, m0 + 32 * wq);
+              else tma_store_2d(&g.tmCt[tl.prob], sb, n0 + c0, m0 + 32 * wq);
+            }
+            if (lane == 0) bulk_commit();
+            ++nstore;
+            buf ^= 1;
+            return;
           }
           if (P.c_trans && P.out_bf16) {
             // a warp's 32 lanes fill one 64-byte row: conflict-free

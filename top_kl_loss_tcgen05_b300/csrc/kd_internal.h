@@ -26,6 +26,9 @@ struct Problem {
   int reduce_add;   // fp32 epilogue: 1 = TMA reduce-add into C, 0 = store
   int c_trans;      // fp32 epilogue: 1 = write C^T (TMEM lanes are C's columns)
   int out_bf16;     // transposed epilogue: 1 = C is bf16 (64-byte boxes, no swizzle), 0 = fp32
+  int bnh;          // wide pair tiles: N of one MMA instruction, the width of each of the
+                    // tile's two halves. 256 (0 means 256), or 240 for 480-wide tiles
+                    // (plain fp32 C only; the last 16 columns of a half use tmCt)
 };
 
 // Kernel parameters (passed as __grid_constant__; tensor maps live in param space).
@@ -33,6 +36,7 @@ struct GemmArgs {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
   CUtensorMap tmC[2];
+  CUtensorMap tmCt[2];    // C with 16-column boxes (no swizzle), for halves 240 wide
   Problem pr[2];
   int nprob;
   int total_tiles;
