@@ -19,9 +19,11 @@
 //              instruction) into one of two TMEM accumulators.
 //              tcgen05.commit frees the smem stage, and then signals the
 //              finished accumulator.
-//   warps 2-5  epilogue: tcgen05.ld the accumulator (each warp owns 32 TMEM
-//              lanes = 32 rows). While the MMA warp fills the other
-//              accumulator, they run the fused math:
+//   warps 2+   epilogue: tcgen05.ld the accumulator (a warp may read only
+//              its quadrant of 32 TMEM lanes = 32 rows; see the widths below
+//              for how many warps share a quadrant). While the MMA warp fills
+//              the other accumulator (narrow tiles) or after it finished
+//              (wide tiles), they run the fused math:
 //     EPI_FWD   online (max, sum exp) per row over the tile's vocabulary
 //               slice, and the logits at the teacher ids that fall in it;
 //     EPI_DZ    dz = s (exp(z - lse) - p [j in K]) -> bf16 -> TMA store;
@@ -49,11 +51,14 @@
 //               48 bytes of operands per 1024 MMA cycles instead of 64, and
 //               operand supply is what limits the narrow tile on B300
 //               (8192^3: 1643 vs 1480 TF/s). The 512-column accumulator
-//               fills TMEM, so the epilogue runs between tiles; eight
-//               epilogue warps (two per TMEM lane quadrant, one per
-//               256-column half) keep that short. Measured per GEMM, the
-//               wide tile pays off for all of them, the dz recompute
-//               included (by about 2%).
+//               fills TMEM, so the epilogue runs between tiles. Sixteen
+//               epilogue warps (four per TMEM lane quadrant, 128 columns
+//               each) keep it short for the forward, dz and store-exp
+//               epilogues; the pair of warps on one 256-column half merge
+//               their row statistics through shared memory. The fp32-store
+//               epilogues (dH / dW, teacher logits) use eight warps with two
+//               staging buffers each. Measured per GEMM, the wide tile pays
+//               off for all of them, the dz recompute included.
 // The logits tile therefore never leaves the chip in the forward pass. In
 // backward, only the chunk's dz (bf16, c x V) goes to HBM.
 #include <atomic>
@@ -80,16 +85,31 @@ struct Cfg {
   static constexpr int TM = C2 ? 2 * kBM : kBM;       // rows of a tile
   static constexpr int TN = W ? 2 * BN : BN;          // columns of a tile
   static constexpr int NACC = W ? 1 : 2;              // TMEM accumulators (512 columns in all)
-  static constexpr int EPI_WARPS = W ? 8 : 4;         // two per TMEM lane quadrant when wide
+  // Epilogue warps. Wide tiles: four per TMEM lane quadrant (each on 128 of
+  // the tile's 512 columns, one staging buffer each) for the epilogues that
+  // keep statistics or store bf16 (forward, dz, store-exp); two per quadrant
+  // (each on a 256-column half, two staging buffers each) for the ones that
+  // store the fp32 tile (dH / dW, teacher logits), which lose more to single
+  // buffering than they gain from more warps. One per quadrant otherwise.
+  static constexpr int EPI_WARPS = W ? ((EPI == EPI_GRAD || EPI == EPI_TEACHER) ? 8 : 16) : 4;
+  static constexpr int SUBS = W ? EPI_WARPS / 8 : 1;  // warps per 256-column half and quadrant
+  static constexpr int SW = BN / SUBS;                // accumulator columns per warp and half
+  static constexpr uint32_t NBUF = SUBS == 2 ? 1u : 2u;  // staging buffers per epilogue warp
+  static constexpr bool DB = EPI_WARPS < 16;          // double-buffered TMEM loads (registers allow)
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer + MMA + epilogue warps
   static constexpr int BNL = (C2 && !WIDE) ? 128 : 256;  // B rows held by one CTA per K step
   static constexpr uint32_t A_BYTES = kBM * kBK * 2;  // this CTA's A block
   static constexpr uint32_t B_BYTES = BNL * kBK * 2;  // this CTA's B block
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
   static constexpr uint32_t TX = C2 ? 2 * STAGE : STAGE;  // bytes that complete one full-barrier phase
-  static constexpr uint32_t STG = (EPI == EPI_FWD) ? 0u : (uint32_t)EPI_WARPS * 2u * kStageBytesStaging;
+  static constexpr uint32_t STG = (EPI == EPI_FWD) ? 0u : (uint32_t)EPI_WARPS * NBUF * kStageBytesStaging;
   static constexpr uint32_t BAR_OFF = NS * STAGE + STG;
-  static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+  // With four warps per quadrant, the two warps that share a 256-column half
+  // combine their per-row statistics through XCH: 16 pair barriers
+  // [kind][half][quadrant], then [kind][half][quadrant][warp][2][32] floats.
+  static constexpr uint32_t XCH_OFF = BAR_OFF + 256;
+  static constexpr uint32_t XCH = SUBS == 2 ? 128u + 2u * 2u * 4u * 2u * 64u * 4u : 0u;
+  static constexpr uint32_t SMEM = XCH_OFF + XCH + 1024;  // + alignment slack
   static_assert((2 * NS + 13) * 8 + 24 <= 256, "barrier block");
 };
 
@@ -127,8 +147,17 @@ __device__ __forceinline__ int lower_bound(const int* rid, int cnt, int x) {
 // at a time (v: lane i holds row i's 32 fp32 values at columns c0 ...
 // c0 + 31). The load of the next 32 columns is in flight while f works on
 // the current ones (two register buffers). ncols is warp-uniform.
-template <typename F>
+template <bool DB = true, typename F>
 __device__ __forceinline__ void tmem_sweep(uint32_t taddr, int ncols, F&& f) {
+  if (!DB) {  // one register buffer (for register-tight launches)
+    uint32_t v[32];
+    for (int c0 = 0; c0 < ncols; c0 += 32) {
+      tmem_ld32(taddr + (uint32_t)c0, v);
+      tmem_wait_ld_r(v);
+      f(v, c0);
+    }
+    return;
+  }
   uint32_t va[32], vb[32];
   const int nch = (ncols + 31) >> 5;
   if (nch <= 0) return;
@@ -286,6 +315,8 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
     }
     mbar_init(drain, 1);
     for (int q = 0; q < 4; ++q) { mbar_init(&tqf[q], 1); mbar_init(&tqe[q], kQueueReaders); }
+    if (C::SUBS == 2)
+      for (int q = 0; q < 16; ++q) mbar_init(reinterpret_cast<uint64_t*>(smem + C::XCH_OFF) + q, 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -466,12 +497,52 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int wq = warp & 3;        // TMEM lane quadrant this warp may access
     const int ew = warp - 2;        // epilogue warp index
-    const int hc = C::W ? ew >> 2 : 0;  // wide: the 256-column half of the tile this warp covers
+    // Column block of this warp: wide tiles give each quadrant four warps,
+    // one per 128 columns (hc = which 256-column half, sub = which 128
+    // columns of it); otherwise one warp covers the 256-column tile.
+    const int hc = (ew >> 2) / C::SUBS;
+    const int sub = (ew >> 2) % C::SUBS;
     int acc = 0;
     uint32_t acc_phase = 0;
     int buf = 0, nstore = 0;
     bool ok = true;
-    uint8_t* stg = smem + NS * C::STAGE + (uint32_t)ew * 2u * kStageBytesStaging;
+    uint8_t* stg = smem + NS * C::STAGE + (uint32_t)ew * C::NBUF * kStageBytesStaging;
+    // The staging buffer for the next TMA store box, once the store that last
+    // used it has finished reading it.
+    auto stage_buf = [&]() -> uint32_t {
+      if (nstore >= (int)C::NBUF) {
+        if (lane == 0) {
+          if (C::NBUF == 2) bulk_wait_read<1>();
+          else bulk_wait_read<0>();
+        }
+        __syncwarp();
+      }
+      return smem_u32(stg + buf * kStageBytesStaging);
+    };
+    auto stage_issued = [&]() {
+      ++nstore;
+      buf = (buf + 1) % (int)C::NBUF;
+    };
+    uint64_t* pbar = reinterpret_cast<uint64_t*>(smem + C::XCH_OFF);  // [kind][half][quadrant]
+    float* xch = reinterpret_cast<float*>(smem + C::XCH_OFF + 128);    // [kind][half][quadrant][warp][2][32]
+    // Wide tiles: hand two values of this row to the other warp of the same
+    // quadrant and half, and take its two (po). `kind` selects one of two
+    // barriers and buffers, so a tile can exchange twice. Bounded: false on
+    // a timeout or an abort.
+    auto pair_exchange = [&](int kind, float a, float b, float* po) -> bool {
+      float* base = xch + ((kind * 2 + hc) * 4 + wq) * 2 * 64;
+      float* mine = base + sub * 64;
+      const float* other = base + (sub ^ 1) * 64;
+      mine[lane] = a;
+      mine[32 + lane] = b;
+      __syncwarp();
+      uint64_t* bar = pbar + (kind * 2 + hc) * 4 + wq;
+      if (lane == 0) mbar_arrive(bar);
+      const bool w = mbar_wait<false>(bar, acc_phase, abort_flag);
+      po[0] = other[lane];
+      po[1] = other[32 + lane];
+      return w;
+    };
     for (int j = 0;; ++j) {
       const int qs = j & 3;
       if (!mbar_wait<C2>(&tqf[qs], (uint32_t)(j >> 2) & 1u, abort_flag)) ok = false;
@@ -490,18 +561,21 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
       const int row = m0 + 32 * wq + lane;
       const int vt = tl.nb * (C::TN / BN) + hc;  // the 256-column block (vocabulary tile) of this warp
       const int bnh = (C::W && P.bnh) ? P.bnh : BN;  // columns of this warp's half (256, or 240)
-      const int n0 = vt * bnh;
+      const int n0 = vt * bnh;                       // first column of the half
+      const int c_sub = sub * C::SW;                 // this warp's first column within the half
+      const int nw0 = n0 + c_sub;                    // ... and in C
+      const int sw = min(C::SW, bnh - c_sub);        // this warp's columns of the half
 
-      // Teacher-id cursor of this row for the tile's vocabulary slice.
+      // Teacher-id cursor of this row for the warp's vocabulary columns.
       int cnt = 0, k = 0;
       const int* rid = nullptr;
       int nvalid = 0;
       if (EPI != EPI_GRAD) {
-        nvalid = min(BN, g.V - n0);
+        nvalid = min(sw, g.V - nw0);
         if (row < g.rows) {
           cnt = __ldg(g.cnt + row);
           rid = g.ids_sorted + (size_t)row * g.Kp;
-          k = lower_bound(rid, cnt, n0);
+          k = lower_bound(rid, cnt, nw0);
         }
       }
 
@@ -509,29 +583,48 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)((acc + hc) * BN);
+      const uint32_t taddr =
+          tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)((acc + hc) * BN) + (uint32_t)c_sub;
       // The loss epilogues work on z / tau: exp arguments use zl2 = log2(e) / tau
       // and the values they keep (tile maxima, logits at teacher ids) are
       // scaled by zscale = 1 / tau. With tau = 1 this is the plain logit.
       const float zscale = g.zscale, zl2 = zscale * kLog2e;
 
-      // Next teacher id of this row inside the tile (kNone if none).
-      const uint32_t hiend = (uint32_t)(n0 + nvalid);
+      // Next teacher id of this row inside the warp's columns (kNone if none).
+      const uint32_t hiend = (uint32_t)(nw0 + nvalid);
       auto next_id = [&]() -> uint32_t {
         return (k < cnt && (uint32_t)__ldg(rid + k) < hiend) ? (uint32_t)__ldg(rid + k) : kNone;
       };
+      // Per-(row, vocabulary tile) statistics: m in units of z and s = sum
+      // exp2((z - m) * l2). Wide tiles first combine the two warps of the
+      // half (the one with sub = 0 writes).
+      auto write_stats = [&](float m, float s, float l2, float mscale) -> bool {
+        if (C::SUBS == 2) {
+          float po[2];
+          const bool w = pair_exchange(1, m, s, po);
+          if (!__all_sync(0xffffffffu, w)) return false;
+          if (sub != 0) return true;
+          const float M = fmaxf(m, po[0]);
+          float S = 0.f;
+          if (m > -INFINITY) S += s * ex2((m - M) * l2);
+          if (po[0] > -INFINITY) S += po[1] * ex2((po[0] - M) * l2);
+          m = M;
+          s = S;
+        }
+        if (row < g.rows && n0 < g.V) {
+          g.part_m[(size_t)row * g.S + vt] = m * mscale;
+          g.part_s[(size_t)row * g.S + vt] = s;
+        }
+        return true;
+      };
 
       if (EPI == EPI_TEACHER) {
-        // Online (max, sum exp) over the tile's valid columns, 32 at a time,
-        // and each 32 x 32 fp32 block stored as it is read.
+        // Online (max, sum exp) over the valid columns, 32 at a time, and
+        // each 32 x 32 fp32 block stored as it is read.
         float m = -INFINITY, s = 0.f;
         const bool box_live = m0 + 32 * wq < g.rows;
-        tmem_sweep(taddr, nvalid, [&](uint32_t (&v)[32], int c0) {
-          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
-          if (nstore >= 2) {
-            if (lane == 0) bulk_wait_read<1>();
-            __syncwarp();
-          }
+        tmem_sweep<C::DB>(taddr, nvalid, [&](uint32_t (&v)[32], int c0) {
+          const uint32_t sb = stage_buf();
           const int lim = nvalid - c0;
           const float mn = fmaxf(m, max32_lim(v, lim));
           const float acc_s = sumexp32_lim(v, lim, kLog2e, -mn * kLog2e);
@@ -542,26 +635,31 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
             st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, n0 + c0, m0 + 32 * wq);
+          if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, nw0 + c0, m0 + 32 * wq);
           if (lane == 0) bulk_commit();
-          ++nstore;
-          buf ^= 1;
+          stage_issued();
         });
-        if (row < g.rows && n0 < g.V) {
-          g.part_m[(size_t)row * g.S + vt] = m;
-          g.part_s[(size_t)row * g.S + vt] = s;
-        }
+        if (!write_stats(m, s, kLog2e, 1.f)) { ok = false; break; }
       } else if (EPI == EPI_FWDST || EPI == EPI_DZ) {
-        // Pass over the tile storing bf16 values, 64 columns per TMA box
-        // (columns past V are clipped by the store):
-        //   EPI_FWDST  e = exp((z - m) / tau), m = the row's tile maximum
-        //              (a first pass), summed in fp32; and z at the teacher
-        //              ids (fp32, from the registers);
+        // Pass over the warp's columns storing bf16 values, 64 columns per
+        // TMA box (columns past V are clipped by the store):
+        //   EPI_FWDST  e = exp((z - m) / tau), m = the row's maximum over the
+        //              256-column tile (a first pass; on wide tiles over both
+        //              warps of the half), summed in fp32; and z at the
+        //              teacher ids (fp32, from the registers);
         //   EPI_DZ     dz = s (exp(z / tau - lse) - p [j in K]); at a teacher
         //              id the difference is formed in fp32 and rounded once.
         float m = -INFINITY;
-        if (EPI == EPI_FWDST)
-          tmem_sweep(taddr, nvalid, [&](uint32_t (&v)[32], int c0) { m = fmaxf(m, max32_lim(v, nvalid - c0)); });
+        if (EPI == EPI_FWDST) {
+          tmem_sweep<C::DB>(taddr, nvalid,
+                            [&](uint32_t (&v)[32], int c0) { m = fmaxf(m, max32_lim(v, nvalid - c0)); });
+          if (C::SUBS == 2) {
+            float po[2];
+            const bool w = pair_exchange(0, m, 0.f, po);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            m = fmaxf(m, po[0]);
+          }
+        }
         float sc = 0.f, nb = 0.f;
         if (EPI == EPI_DZ) {
           const float lse_r = (row < g.rows) ? __ldg(g.lse + row) : 0.f;
@@ -575,15 +673,9 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
         const bool box_live = m0 + 32 * wq < g.rows;
         uint32_t want = next_id();
         uint32_t sb = 0;
-        tmem_sweep(taddr, nvalid, [&](uint32_t (&v)[32], int c0) {
+        tmem_sweep<C::DB>(taddr, nvalid, [&](uint32_t (&v)[32], int c0) {
           const int h = (c0 >> 5) & 1;  // which half of the 64-column box
-          if (h == 0) {
-            sb = smem_u32(stg + buf * kStageBytesStaging);
-            if (nstore >= 2) {
-              if (lane == 0) bulk_wait_read<1>();
-              __syncwarp();
-            }
-          }
+          if (h == 0) sb = stage_buf();
           const int lim = nvalid - c0;
           uint32_t pk[16];
 #pragma unroll
@@ -608,7 +700,7 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
                          pk[4 * qq + 3]);
           }
           // Teacher ids in these 32 columns, from the fp32 logits in registers.
-          const uint32_t lo = (uint32_t)(n0 + c0);
+          const uint32_t lo = (uint32_t)(nw0 + c0);
           bool mine = want < lo + 32u;
           while (__any_sync(0xffffffffu, mine)) {
             if (mine) {
@@ -632,28 +724,39 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
           if (h == 1 || c0 + 32 >= nvalid) {  // the 64-column box is complete
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, n0 + c0 - 32 * h, m0 + 32 * wq);
+            if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, nw0 + c0 - 32 * h, m0 + 32 * wq);
             if (lane == 0) bulk_commit();
-            ++nstore;
-            buf ^= 1;
+            stage_issued();
           }
         });
-        if (EPI == EPI_FWDST && row < g.rows && n0 < g.V) {
-          g.part_m[(size_t)row * g.S + vt] = m * zscale;
-          g.part_s[(size_t)row * g.S + vt] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        if (EPI == EPI_FWDST) {
+          // the sums are relative to the common maximum m: the pair just adds
+          float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          bool write = true;
+          if (C::SUBS == 2) {
+            float po[2];
+            const bool w = pair_exchange(1, s, 0.f, po);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            s += po[0];
+            write = sub == 0;
+          }
+          if (write && row < g.rows && n0 < g.V) {
+            g.part_m[(size_t)row * g.S + vt] = m * zscale;
+            g.part_s[(size_t)row * g.S + vt] = s;
+          }
         }
       } else if (EPI == EPI_FWD) {
-        // Online (max, sum exp) per row over the tile's vocabulary slice, and
-        // the logits at the teacher ids that fall in it.
+        // Online (max, sum exp) per row over the warp's columns, and the
+        // logits at the teacher ids that fall in them.
         float m = -INFINITY, s = 0.f;
         uint32_t want = next_id();
-        tmem_sweep(taddr, nvalid, [&](uint32_t (&v)[32], int c0) {
+        tmem_sweep<C::DB>(taddr, nvalid, [&](uint32_t (&v)[32], int c0) {
           const int lim = nvalid - c0;
           const float mn = fmaxf(m, max32_lim(v, lim));
           const float acc_s = sumexp32_lim(v, lim, zl2, -mn * zl2);
           s = s * ex2((m - mn) * zl2) + acc_s;
           m = mn;
-          const uint32_t lo = (uint32_t)(n0 + c0);
+          const uint32_t lo = (uint32_t)(nw0 + c0);
           bool mine = want < lo + 32u;
           while (__any_sync(0xffffffffu, mine)) {
             if (mine) {
@@ -664,24 +767,17 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
             }
           }
         });
-        if (row < g.rows && n0 < g.V) {
-          g.part_m[(size_t)row * g.S + vt] = m * zscale;
-          g.part_s[(size_t)row * g.S + vt] = s;
-        }
+        if (!write_stats(m, s, zl2, zscale)) { ok = false; break; }
       } else {
         // EPI_GRAD: the fp32 tile, 32 columns per TMA box, stored or
         // reduce-added into C, or written as C^T (TMEM lanes are then C's
         // columns): fp32, or bf16 in 64-byte rows without swizzle.
         const CUtensorMap* mC = &g.tmC[tl.prob];
         const bool box_live = m0 + 32 * wq < P.M;
-        const int ncols = min(bnh, P.N - n0);
-        tmem_sweep(taddr, ncols, [&](uint32_t (&v)[32], int c0) {
-          const uint32_t sb = smem_u32(stg + buf * kStageBytesStaging);
-          if (nstore >= 2) {
-            if (lane == 0) bulk_wait_read<1>();
-            __syncwarp();
-          }
-          if (c0 + 32 > bnh) {
+        const int ncols = min(sw, P.N - nw0);
+        tmem_sweep<C::DB>(taddr, ncols, [&](uint32_t (&v)[32], int c0) {
+          const uint32_t sb = stage_buf();
+          if (c_sub + c0 + 32 > bnh) {
             // the last 16 columns of a 240-wide half (plain fp32 C): a 16-column
             // box, so nothing is stored into the neighbouring tile's columns
 #pragma unroll
@@ -690,12 +786,11 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && box_live) {
-              if (P.reduce_add) tma_reduce_add_2d(&g.tmCt[tl.prob], sb, n0 + c0, m0 + 32 * wq);
-              else tma_store_2d(&g.tmCt[tl.prob], sb, n0 + c0, m0 + 32 * wq);
+              if (P.reduce_add) tma_reduce_add_2d(&g.tmCt[tl.prob], sb, nw0 + c0, m0 + 32 * wq);
+              else tma_store_2d(&g.tmCt[tl.prob], sb, nw0 + c0, m0 + 32 * wq);
             }
             if (lane == 0) bulk_commit();
-            ++nstore;
-            buf ^= 1;
+            stage_issued();
             return;
           }
           if (P.c_trans && P.out_bf16) {
@@ -719,15 +814,14 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && box_live) {
-            if (P.c_trans && P.out_bf16) tma_store_2d(mC, sb, m0 + 32 * wq, n0 + c0);
-            else if (P.c_trans && P.reduce_add) tma_reduce_add_2d(mC, sb, m0 + 32 * wq, n0 + c0);
-            else if (P.c_trans) tma_store_2d(mC, sb, m0 + 32 * wq, n0 + c0);
-            else if (P.reduce_add) tma_reduce_add_2d(mC, sb, n0 + c0, m0 + 32 * wq);
-            else tma_store_2d(mC, sb, n0 + c0, m0 + 32 * wq);
+            if (P.c_trans && P.out_bf16) tma_store_2d(mC, sb, m0 + 32 * wq, nw0 + c0);
+            else if (P.c_trans && P.reduce_add) tma_reduce_add_2d(mC, sb, m0 + 32 * wq, nw0 + c0);
+            else if (P.c_trans) tma_store_2d(mC, sb, m0 + 32 * wq, nw0 + c0);
+            else if (P.reduce_add) tma_reduce_add_2d(mC, sb, nw0 + c0, m0 + 32 * wq);
+            else tma_store_2d(mC, sb, nw0 + c0, m0 + 32 * wq);
           }
           if (lane == 0) bulk_commit();
-          ++nstore;
-          buf ^= 1;
+          stage_issued();
         });
       }
       // Release the accumulator (C2: the even CTA's barrier counts both CTAs).
