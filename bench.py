@@ -241,15 +241,19 @@ def cpu_workload(wl):
 
 
 def size_sample(cw, budget_s: float) -> int:
-    """Rows of oracle work that take about budget_s: time(r) = a + b r is
-    fitted from 2 and 8 rows after a warm-up call (a is the per-call cost,
-    e.g. allocating the fp64 dW)."""
-    oracle_sample(cw, 2)
-    t2 = oracle_sample(cw, 2)
-    t8 = oracle_sample(cw, 8)
-    b = max((t8 - t2) / 6.0, 1e-6)
-    a = max(t2 - 2.0 * b, 0.0)
-    return int(max(2, min(len(cw["ids"]), (budget_s - a) / b)))
+    """Rows of oracle work that take at most about budget_s. Rows double from
+    4 until one call takes a third of the budget (or all rows are in), then
+    scale to the budget from that last measurement. With time(r) = a + b r
+    and a >= 0 (a per-call cost, e.g. allocating the fp64 dW), scaling the
+    rows by budget / time(r) cannot overshoot the budget."""
+    cap = len(cw["ids"])
+    oracle_sample(cw, 2)  # warm-up
+    r = min(4, cap)
+    t = oracle_sample(cw, r)
+    while t < budget_s / 3.0 and r < cap:
+        r = min(cap, 2 * r)
+        t = oracle_sample(cw, r)
+    return int(max(2, min(cap, r * budget_s / max(t, 1e-6))))
 
 
 def cpu_baseline(wl, budget_s: float = 15.0):

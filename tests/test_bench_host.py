@@ -118,3 +118,25 @@ def test_roofline_fields_from_a_profile():
 
 def test_max_over_ranks_single_process():
     assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+@pytest.mark.parametrize("a,b,cap", [(0.0, 0.01, 4096), (5.0, 0.01, 4096), (0.5, 0.2, 4096), (0.0, 1e-5, 300)])
+def test_oracle_sample_sizing_never_overshoots(monkeypatch, a, b, cap):
+    """size_sample picks rows whose oracle time stays within the budget for
+    any per-call cost a >= 0 and per-row cost b (time = a + b r), and never
+    more rows than the sample holds."""
+    calls = []
+
+    def fake(cw, rows):
+        calls.append(rows)
+        return a + b * rows
+
+    monkeypatch.setattr(bench, "oracle_sample", fake)
+    budget = 6.0
+    rows = bench.size_sample({"ids": [0] * cap}, budget)
+    assert 2 <= rows <= cap
+    if a < budget:
+        assert a + b * rows <= budget * 1.0001
+    if a + b * cap <= budget / 3:
+        assert rows == cap
+    assert sum(a + b * r for r in calls) < 4 * budget + 10 * a  # probing stays bounded
