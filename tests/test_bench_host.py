@@ -140,3 +140,12 @@ def test_oracle_sample_sizing_never_overshoots(monkeypatch, a, b, cap):
     if a + b * cap <= budget / 3:
         assert rows == cap
     assert sum(a + b * r for r in calls) < 4 * budget + 10 * a  # probing stays bounded
+
+
+def test_workload_description_names_a_truncated_run():
+    """A --rows capture run says it covers only the first positions; the
+    full workload's description is the plain shape."""
+    assert bench.describe("long") == "long: T=262144 d=2880 V=201088 K=100 chunk=4096"
+    d = bench.describe("long", 8192)
+    assert d.startswith("long: T=8192 d=2880 V=201088 K=100 chunk=4096") and "first 8192 of its 262144" in d
+    assert bench.describe("tiny", 10**9) == bench.describe("tiny")
