@@ -16,7 +16,9 @@
 //              a 4-deep shared-memory queue, and streams the tile's A/B
 //              blocks into a ring of shared-memory stages (128-byte swizzle).
 //   warp 1     MMA issuer: one thread issues tcgen05.mma (K = 16 per
-//              instruction) into one of two TMEM accumulators.
+//              instruction) into one of two 256-column TMEM accumulators, or
+//              (wide tiles) into one 512-column accumulator, two MMAs per K
+//              step that share their A operand.
 //              tcgen05.commit frees the smem stage, and then signals the
 //              finished accumulator.
 //   warps 2+   epilogue: tcgen05.ld the accumulator (a warp may read only
