@@ -131,7 +131,8 @@ KD_API int kd_topk_cache(const void* logits, int32_t dtype, int64_t T, int64_t V
  * Requires d % 8 == 0, 16-byte aligned H and W, 1 <= K <= min(V, 65536).
  * Workspace: kd_teacher_topk_workspace_size(d, V, K, chunk) bytes
  * (4 * chunk * round_up(V, 64) for the logits of one chunk, plus 8 bytes per
- * position and vocabulary tile; independent of T). Its first two int32
+ * position and vocabulary tile; independent of T; 0 for sizes the call
+ * refuses). Its first two int32
  * words are the status word and the running count of rows that took the
  * exact radix path (see kd_topk_cache). This is the teacher-side fusion
  * that the offline step needs ([KD-TH] section "การทำ Distillation แบบ
@@ -191,7 +192,8 @@ KD_API int kd_topk_cache_noalloc(const void* logits, int32_t dtype, int64_t T, i
  *   default group, kd_fused_kl_workspace_size_ex(d, V, K, chunk, group) for
  *   an explicit one (group = 0 is the default). It does not depend on T; one
  *   workspace serves all three calls made with the same group. Both return 0
- *   for a non-positive size or a negative group.
+ *   for a non-positive size, a negative group, or any size the calls refuse
+ *   (K > 4096 or K > V, V >= 2^31, d, chunk or group * chunk above 2^24).
  */
 KD_API size_t kd_fused_kl_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk);
 KD_API size_t kd_fused_kl_workspace_size_ex(int64_t d, int64_t V, int32_t K, int64_t chunk, int32_t group);

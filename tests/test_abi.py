@@ -223,3 +223,20 @@ def test_noalloc_refuses_before_touching_the_stream(lib):
     assert call(P16, 0, 4, 1 << 31, 1 << 31, 2, P16, P16, None) == _native.KD_ERR_UNSUPPORTED  # V
     assert call(P16, 0, 4, 70000, 70000, 65537, P16, P16, None) == _native.KD_ERR_UNSUPPORTED  # K
     assert call(P16, 0, 4, 8, 8, 9, P16, P16, None) == _native.KD_ERR_INVALID_ARG
+
+
+def test_workspace_queries_refuse_what_the_calls_refuse(lib):
+    """Size queries return 0, not a wrapped-around size, for shapes the calls
+    would refuse."""
+    f = lib.kd_fused_kl_workspace_size_ex
+    assert f(2880, 201088, 100, 4096, 0) > 0
+    assert f(2880, 201088, 100, 1 << 25, 0) == 0            # chunk above 2^24
+    assert f(2880, 201088, 100, 1 << 20, 64) == 0           # group * chunk above 2^24
+    assert f(2880, 201088, 100, 4096, (1 << 31) - 1) == 0   # absurd group
+    assert f(2880, 201088, 5000, 4096, 0) == 0              # K > 4096
+    assert f(2880, 100, 101, 64, 0) == 0                    # K > V
+    assert f(1 << 25, 1000, 10, 64, 0) == 0                 # d above 2^24
+    assert lib.kd_fused_kl_workspace_size(2880, 1 << 31, 100, 4096) == 0
+    t = lib.kd_teacher_topk_workspace_size
+    assert t(4096, 128256, 100, 1024) > 0
+    assert t(4096, 128256, 100, 1 << 25) == 0 and t(4096, 100, 101, 64) == 0 and t(4096, 1 << 31, 10, 64) == 0

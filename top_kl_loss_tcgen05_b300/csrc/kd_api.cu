@@ -528,6 +528,11 @@ int kd_topk_cache(const void* logits, int32_t dtype, int64_t T, int64_t V, int64
 
 size_t kd_fused_kl_workspace_size_ex(int64_t d, int64_t V, int32_t K, int64_t chunk, int32_t group) {
   if (d <= 0 || V <= 0 || K <= 0 || chunk <= 0 || group < 0) return 0;
+  // Sizes the calls refuse get no workspace size either (and the layout
+  // arithmetic stays far from overflow).
+  if (K > 4096 || K > V || V >= (int64_t(1) << 31) || d > (int64_t(1) << 24) || chunk > (int64_t(1) << 24) ||
+      bwd_group(chunk, group) * chunk > (int64_t(1) << 24))
+    return 0;
   return fused_layout(d, V, K, chunk, group).total;
 }
 
@@ -722,6 +727,8 @@ int kd_fused_kl_fwdbwd(const void* H, const void* W, const int32_t* ids, const f
 
 size_t kd_teacher_topk_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk) {
   if (d <= 0 || V <= 0 || K <= 0 || chunk <= 0) return 0;
+  if (K > V || K > 65536 || V >= (int64_t(1) << 31) || d > (int64_t(1) << 24) || chunk > (int64_t(1) << 24))
+    return 0;
   return teacher_layout(V, chunk).total;
 }
 
