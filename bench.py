@@ -391,9 +391,9 @@ def run_reference(args, world, rank):
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     name = args.workload
     c = synth.CONFIGS[name]
-    # inputs drawn exactly as for the GPU arm (the cache from the synthetic
-    # perturbed teacher is not needed to time the oracle: a synthetic cache of
-    # the same shape is used so this arm runs without the GPU path)
+    # inputs of the GPU arm's shapes and distributions, drawn on the host for
+    # the first (at most 4096) positions; a synthetic cache of the same shape
+    # stands in for the teacher's, so this arm runs without the GPU path
     H, W = synth.student(min(c["T"], 4096), c["d"], c["V"], c["seed"], device="cpu")
     ids, logp = synth.synthetic_cache(min(c["T"], 4096), c["V"], c["K"], c["seed"])
     cw = dict(T=c["T"], H=H.float().numpy().astype(np.float64), W64=W.float().numpy().astype(np.float64),

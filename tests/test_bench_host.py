@@ -4,7 +4,6 @@ the description of the GEMM tile shapes."""
 
 import json
 import os
-import shutil
 import sys
 
 import pytest

@@ -2,7 +2,6 @@
 oracle: one position, K = 1, chunk = 1 and chunk > T, the smallest d, the
 largest supported K, and argument errors returned before any launch."""
 
-import ctypes
 
 import numpy as np
 import pytest

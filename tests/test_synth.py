@@ -3,7 +3,6 @@ the design notes state: the distributions, the per-row Zipf-like bias of the
 top-K workload, the synthetic cache's distinct ids, determinism by seed, and
 slices of the top-K workload that match the full draw."""
 
-import math
 
 import numpy as np
 import pytest

@@ -1,8 +1,6 @@
 """kd_topk_cache against the fp64 oracle: ids bit-exact (value descending,
 ties to the lowest id), log-softmax within 1e-4 absolute."""
 
-import os
-
 import numpy as np
 import pytest
 import torch
