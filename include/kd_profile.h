@@ -7,6 +7,13 @@
  * name, the number of launches and their summed device time. The events are
  * created on the host; no device memory is allocated. When profiling is off
  * (the default), launches record nothing.
+ *
+ * Independently of these calls, every compute call of the C ABI runs inside
+ * an NVTX range named after it ("kd_fused_kl_fwd", "kd_topk_cache", ...), and
+ * each of its kernel launches inside a nested range named as in the entries
+ * below (e.g. "grad_dH_dW"). A tool such as ncu can select launches by these
+ * ranges (--nvtx --nvtx-include "kd_fused_kl_bwd/grad_dH_dW/"). With no tool
+ * attached the ranges cost a pointer check each.
  */
 #ifndef KD_PROFILE_H_
 #define KD_PROFILE_H_

@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/kd.h"
 #include "../../include/kd_profile.h"
@@ -203,24 +204,38 @@ cudaEvent_t prof_event() {
   return e;
 }
 
-// Records an event before the launch (constructor) and after it (destructor)
-// on the launch stream, while profiling is on.
+// Brackets one kernel launch: an NVTX range named after the kernel (a
+// pointer check when no tool is attached), and, while profiling is on, an
+// event recorded on the launch stream before the launch (constructor) and
+// after it (destructor).
 struct ProfScope {
   int kid;
   cudaStream_t s;
   cudaEvent_t a = nullptr;
   ProfScope(int k, cudaStream_t st) : kid(k), s(st) {
+    nvtxRangePushA(kKernelNames[k]);
     std::lock_guard<std::mutex> g(g_prof_mu);
     if (!g_prof_on) return;
     a = prof_event();
     if (a && cudaEventRecord(a, s) != cudaSuccess) a = nullptr;
   }
   ~ProfScope() {
-    if (!a) return;
-    std::lock_guard<std::mutex> g(g_prof_mu);
-    cudaEvent_t b = prof_event();
-    if (b && cudaEventRecord(b, s) == cudaSuccess) g_prof_recs.push_back({kid, a, b});
+    if (a) {
+      std::lock_guard<std::mutex> g(g_prof_mu);
+      cudaEvent_t b = prof_event();
+      if (b && cudaEventRecord(b, s) == cudaSuccess) g_prof_recs.push_back({kid, a, b});
+    }
+    nvtxRangePop();
   }
+};
+
+// NVTX range around one call of the C ABI, named after it; the launches of
+// the call nest inside it.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
 };
 
 int cuda_status(cudaError_t e) {
@@ -515,6 +530,7 @@ size_t kd_topk_workspace_size(int64_t T, int64_t V, int32_t K, int32_t dtype) {
 
 int kd_topk_cache(const void* logits, int32_t dtype, int64_t T, int64_t V, int64_t ld, int32_t K, int32_t* ids,
                   float* logp, void* ws, size_t ws_bytes, void* stream) {
+  CallRange call_range("kd_topk_cache");
   const int chk = topk_check_args(logits, dtype, T, V, ld, K, ids, logp);
   if (chk != KD_OK) return chk;
   if (!ws || !aligned(ws, 256) || ws_bytes < kHeader) return KD_ERR_WORKSPACE;
@@ -543,6 +559,7 @@ size_t kd_fused_kl_workspace_size(int64_t d, int64_t V, int32_t K, int64_t chunk
 int kd_fused_kl_fwd_ex(const void* H, const void* W, const int32_t* ids, const float* logp, int64_t T, int64_t d,
                        int64_t V, int32_t K, int64_t chunk, float* loss, float* lse, float* loss_rows,
                        const kd_kl_options* opt, void* ws, size_t ws_bytes, void* stream) {
+  CallRange call_range("kd_fused_kl_fwd");
   LossOpts o;
   int st = parse_opts(opt, &o);
   if (st != KD_OK) return st;
@@ -597,6 +614,7 @@ int kd_fused_kl_bwd_ex(const void* H, const void* W, const int32_t* ids, const f
                        int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk, float grad_scale,
                        const float* grad_scale_dev, void* dH, float* dW, int32_t accumulate_dW,
                        const kd_kl_options* opt, void* ws, size_t ws_bytes, void* stream) {
+  CallRange call_range("kd_fused_kl_bwd");
   LossOpts o;
   int st = parse_opts(opt, &o);
   if (st != KD_OK) return st;
@@ -658,6 +676,7 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
                           int64_t V, int32_t K, int64_t chunk, float grad_scale, const float* grad_scale_dev,
                           float* loss, float* lse, float* loss_rows, void* dH, float* dW, int32_t accumulate_dW,
                           const kd_kl_options* opt, void* ws, size_t ws_bytes, void* stream) {
+  CallRange call_range("kd_fused_kl_fwdbwd");
   LossOpts o;
   int st = parse_opts(opt, &o);
   if (st != KD_OK) return st;
@@ -734,6 +753,7 @@ size_t kd_teacher_topk_workspace_size(int64_t d, int64_t V, int32_t K, int64_t c
 
 int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_t d, int64_t V, int32_t K, int64_t chunk,
                           int32_t* ids, float* logp, void* ws, size_t ws_bytes, void* stream) {
+  CallRange call_range("kd_teacher_topk_cache");
   if (!H || !W || !ids || !logp || T <= 0 || d <= 0 || V <= 0 || K <= 0 || chunk <= 0 || K > V)
     return KD_ERR_INVALID_ARG;
   if (V >= (int64_t(1) << 31) || K > 65536 || d % 8 != 0 || d > (int64_t(1) << 24) || chunk > (int64_t(1) << 24))
