@@ -211,3 +211,40 @@ def test_group_one_at_llama3b_shape(cuda_dev):
     assert frob(dW2.cpu().numpy(), dW_o) <= GRAD_ACHIEVED
     assert frob(dH2.cpu().numpy(), dH_o) <= GRAD_RTOL
     assert frob(dH2.cpu().numpy(), dH_o) <= GRAD_ACHIEVED
+
+
+def test_full_size_variants_sampled_positions(cuda_dev):
+    """The loss variants at the GPT-OSS-20B shape (T=32768, d=2880, V=201088,
+    K=100, chunk=2048): temperature 2, a seeded mask that drops about one
+    position in ten, and the mean over the included positions. Sampled rows
+    (masked and unmasked among them) against the oracle computing those rows
+    alone: lse of z / tau, L_t (0 where masked) and dH_t (with the factor
+    1/N of the full mask); the scalar loss is the sum of the rows over N."""
+    c, H, W, ids, logp = _inputs("gptoss20b")
+    T, chunk, tau = c["T"], c["chunk"], 2.0
+    g = torch.Generator().manual_seed(77)
+    mask = (torch.rand(T, generator=g) >= 0.1).to(torch.uint8)
+    N = int(mask.sum())
+    m_dev = mask.to(cuda_dev)
+    loss, lse, rows = kd.fused_kl_fwd(H, W, ids, logp, chunk, want_rows=True, temperature=tau, mask=m_dev,
+                                      mean_over_mask=True)
+    dH, _ = kd.fused_kl_bwd(H, W, ids, logp, lse, chunk, 1.0, temperature=tau, mask=m_dev, mean_over_mask=True)
+    torch.cuda.synchronize()
+    rows_g = rows.cpu().numpy().astype(np.float64)
+    assert abs(loss.item() - rows_g.sum() / N) <= 1e-6 * abs(loss.item())
+    S = _sample_rows(T, chunk, n=48, seed=3)
+    mk = mask.numpy()
+    S = np.unique(np.concatenate([S, np.nonzero(mk == 0)[0][:8]]))  # some excluded positions too
+    St = torch.as_tensor(S, device=cuda_dev)
+    Hs = H[St].float().cpu().numpy()
+    W64 = W.float().cpu().numpy().astype(np.float64)
+    ids_s, logp_s = ids[St].cpu().numpy(), logp[St].cpu().numpy()
+    _, lse_o, L_o = O.fused_kl_forward(Hs, W64, ids_s, logp_s, temperature=tau, mask=mk[S])
+    dH_o, _ = O.fused_kl_backward(Hs, W64, ids_s, logp_s, 1.0 / N, temperature=tau, mask=mk[S])
+    np.testing.assert_allclose(lse.cpu().numpy()[S], lse_o, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(rows_g[S], L_o, rtol=LOSS_RTOL, atol=1e-4)
+    assert np.all(rows_g[S][mk[S] == 0] == 0.0)
+    dH_s = dH[St].cpu().numpy()
+    assert np.all(dH_s[mk[S] == 0] == 0.0)
+    assert frob(dH_s, dH_o) <= GRAD_RTOL
+    assert frob(dH_s, dH_o) <= GRAD_ACHIEVED
