@@ -18,7 +18,9 @@
 //   warp 1     MMA issuer: one thread issues tcgen05.mma (K = 16 per
 //              instruction) into one of two 256-column TMEM accumulators, or
 //              (wide tiles) into one 512-column accumulator, two MMAs per K
-//              step that share their A operand.
+//              step that share their A operand: the first keeps A in the
+//              tensor core's collector buffer, the second reads it from
+//              there, so A leaves shared memory once per K step.
 //              tcgen05.commit frees the smem stage, and then signals the
 //              finished accumulator.
 //   warps 2+   epilogue: tcgen05.ld the accumulator (a warp may read only
@@ -256,9 +258,26 @@ __device__ __forceinline__ void tmem_dealloc_x(uint32_t taddr) {
   else
     tmem_dealloc(taddr, kTmemCols);
 }
-template <bool C2>
+// A-operand collector use of one MMA: none, fill (read A from shared memory
+// and keep it), or lastuse (take A kept by the previous MMA, then drop it).
+enum class CollA { kNone, kFill, kLastUse };
+template <bool C2, CollA CA = CollA::kNone>
 __device__ __forceinline__ void mma_x(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
-  if (C2)
+  if (C2 && CA == CollA::kFill)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16.collector::a::fill [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+  else if (C2 && CA == CollA::kLastUse)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16.collector::a::lastuse [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+  else if (C2)
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
@@ -469,9 +488,16 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t ad = P.a_mn ? sdesc_sw128(sA + k * 2048, 8192, 1024) : sdesc_sw128(sA + k * 32, 16, 1024);
             const uint64_t bd = b_mn ? sdesc_sw128(sB + k * 2048, 8192, 1024) : sdesc_sw128(sB + k * 32, 16, 1024);
-            mma_x<C2>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-            if (C::W)  // N half 1: B rows 256 further in smem, TMEM columns 256 further
-              mma_x<C2>(d_tmem + 256, ad, sdesc_sw128(sB + 16384 + k * 32, 16, 1024), idesc, (kb | k) != 0 ? 1u : 0u);
+            if (C::W) {
+              // The two N halves share A: the first MMA keeps it in the
+              // collector, the second (B rows 256 further in smem, TMEM
+              // columns 256 further) reads it from there instead of smem.
+              mma_x<C2, CollA::kFill>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              mma_x<C2, CollA::kLastUse>(d_tmem + 256, ad, sdesc_sw128(sB + 16384 + k * 32, 16, 1024), idesc,
+                                         (kb | k) != 0 ? 1u : 0u);
+            } else {
+              mma_x<C2>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
           }
           commit_x<C2>(&empty[stage]);
           if (++stage == NS) { stage = 0; phase ^= 1u; }
