@@ -151,22 +151,30 @@ __device__ __forceinline__ int lower_bound(const int* rid, int cnt, int x) {
 // at a time (v: lane i holds row i's 32 fp32 values at columns c0 ...
 // c0 + 31). The load of the next 32 columns is in flight while f works on
 // the current ones (two register buffers). ncols is warp-uniform.
-template <bool DB = true, typename F>
-__device__ __forceinline__ void tmem_sweep(uint32_t taddr, int ncols, F&& f) {
+// done() runs once, as soon as the last load has completed (before f works
+// on those columns; at once if there are none): from then on the sweep
+// reads only registers, so the caller may hand the accumulator back there.
+template <bool DB = true, typename F, typename D>
+__device__ __forceinline__ void tmem_sweep(uint32_t taddr, int ncols, F&& f, D&& done) {
+  const int nch = (ncols + 31) >> 5;
+  if (nch <= 0) {
+    done();
+    return;
+  }
   if (!DB) {  // one register buffer (for register-tight launches)
     uint32_t v[32];
-    for (int c0 = 0; c0 < ncols; c0 += 32) {
-      tmem_ld32(taddr + (uint32_t)c0, v);
+    for (int c = 0; c < nch; ++c) {
+      tmem_ld32(taddr + (uint32_t)c * 32u, v);
       tmem_wait_ld_r(v);
-      f(v, c0);
+      if (c + 1 == nch) done();
+      f(v, c * 32);
     }
     return;
   }
   uint32_t va[32], vb[32];
-  const int nch = (ncols + 31) >> 5;
-  if (nch <= 0) return;
   tmem_ld32(taddr, va);
   tmem_wait_ld_r(va);
+  if (nch == 1) done();
   for (int c = 0; c < nch; c += 2) {
     const bool nb = c + 1 < nch;
     if (nb) tmem_ld32(taddr + (uint32_t)(c + 1) * 32u, vb);
@@ -174,11 +182,19 @@ __device__ __forceinline__ void tmem_sweep(uint32_t taddr, int ncols, F&& f) {
     if (nb) {
       tmem_wait_ld_r(vb);
       const bool na = c + 2 < nch;
+      if (!na) done();
       if (na) tmem_ld32(taddr + (uint32_t)(c + 2) * 32u, va);
       f(vb, (c + 1) * 32);
-      if (na) tmem_wait_ld_r(va);
+      if (na) {
+        tmem_wait_ld_r(va);
+        if (c + 3 == nch) done();
+      }
     }
   }
+}
+template <bool DB = true, typename F>
+__device__ __forceinline__ void tmem_sweep(uint32_t taddr, int ncols, F&& f) {
+  tmem_sweep<DB>(taddr, ncols, f, [] {});
 }
 
 // Maximum of the first lim (>= 1) of the 32 values.
@@ -613,6 +629,20 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)((acc + hc) * BN) + (uint32_t)c_sub;
+      // Hands the accumulator back to the MMA warp (C2: the even CTA's
+      // barrier counts both CTAs). The sweeps call it once their last
+      // TMEM load has completed, so the next tile's MMAs run while this
+      // warp finishes its last columns from registers.
+      bool released = false;
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(&tempty[acc]);
+          else mbar_arrive_remote(&tempty[acc], 0);
+        }
+        released = true;
+      };
       // The loss epilogues work on z / tau: exp arguments use zl2 = log2(e) / tau
       // and the values they keep (tile maxima, logits at teacher ids) are
       // scaled by zscale = 1 / tau. With tau = 1 this is the plain logit.
@@ -666,7 +696,7 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
           if (lane == 0 && box_live) tma_store_2d(&g.tmC[0], sb, nw0 + c0, m0 + 32 * wq);
           if (lane == 0) bulk_commit();
           stage_issued();
-        });
+        }, release);
         if (!write_stats(m, s, kLog2e, 1.f)) { ok = false; break; }
       } else if (EPI == EPI_FWDST || EPI == EPI_DZ) {
         // Pass over the warp's columns storing bf16 values, 64 columns per
@@ -756,7 +786,7 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
             if (lane == 0) bulk_commit();
             stage_issued();
           }
-        });
+        }, release);
         if (EPI == EPI_FWDST) {
           // the sums are relative to the common maximum m: the pair just adds
           float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
@@ -794,7 +824,7 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
               mine = want < lo + 32u;
             }
           }
-        });
+        }, release);
         if (!write_stats(m, s, zl2, zscale)) { ok = false; break; }
       } else {
         // EPI_GRAD: the fp32 tile, 32 columns per TMA box, stored or
@@ -850,15 +880,9 @@ __global__ void __launch_bounds__(Cfg<NS, EPI, C2, WIDE>::THREADS, 1)
           }
           if (lane == 0) bulk_commit();
           stage_issued();
-        });
+        }, release);
       }
-      // Release the accumulator (C2: the even CTA's barrier counts both CTAs).
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (leader) mbar_arrive(&tempty[acc]);
-        else mbar_arrive_remote(&tempty[acc], 0);
-      }
+      if (!released) release();  // (every sweep releases; kept as a guard)
       if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
     }
     if (!ok) {
