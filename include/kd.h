@@ -154,9 +154,9 @@ KD_API int kd_teacher_topk_cache(const void* H, const void* W, int64_t T, int64_
  *  - Arguments are checked, as kd_topk_cache checks them, before anything is
  *    enqueued; a refused call leaves the stream untouched.
  *  - The first call on a device looks up that array's device address
- *    (cudaGetSymbolAddress) and keeps it. Make that first call before any
- *    stream capture. The lookup is repeated when the device's context has
- *    changed since (after cudaDeviceReset, for example).
+ *    (cudaGetSymbolAddress, a host call) and keeps it. The lookup is
+ *    repeated when the device's context has changed since (after
+ *    cudaDeviceReset, for example).
  *  - Each call clears the array on `stream`. Calls that overlap on the GPU
  *    (unordered streams) share the array and race on it.
  *  - If the workspace that kd_topk_cache would need exceeds the array, the call
