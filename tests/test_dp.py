@@ -34,8 +34,13 @@ def _inputs(T, d, V, K, seed):
 
 
 def oracle_shard_call(H, W, ids, logp, chunk, s):
-    """The loss on one shard from the oracle (fp64, CPU tensors in and out)."""
+    """The loss on one shard from the oracle (fp64, CPU tensors in and out).
+    Like libkd, it refuses a shard without positions (libkd returns
+    KD_ERR_INVALID_ARG for T = 0), so the helper must not make that call."""
     from oracle import kd_oracle as O
+
+    if H.shape[0] == 0:
+        raise ValueError("the loss refuses T = 0")
 
     Hn, Wn = H.numpy(), W.numpy()
     _, _, L = O.fused_kl_forward(Hn, Wn, ids.numpy(), logp.numpy())
@@ -60,7 +65,7 @@ def _rank_main(rank, world, port, T, q):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("T", [200, 201])
+@pytest.mark.parametrize("T", [200, 201, 1])  # T = 1: rank 1 holds no positions
 def test_two_gloo_ranks_reproduce_the_full_batch_loss_and_gradients(T):
     from oracle import kd_oracle as O
 
@@ -108,3 +113,35 @@ def test_single_rank_without_a_process_group_is_the_plain_loss():
     assert abs(float(loss) - loss_o) <= 1e-6 * abs(loss_o)
     np.testing.assert_allclose(dH.numpy(), dH_o, rtol=1e-12)
     np.testing.assert_allclose(dW.numpy(), dW_o, rtol=1e-12)
+
+
+hypothesis = pytest.importorskip("hypothesis")
+from hypothesis import given, settings  # noqa: E402
+from hypothesis import strategies as st  # noqa: E402
+
+
+@settings(max_examples=25, deadline=None, derandomize=True)
+@given(st.integers(1, 12), st.integers(1, 6), st.floats(0.25, 4.0), st.integers(0, 1000))
+def test_shards_of_any_split_sum_to_the_full_batch(T, world, gscale, seed):
+    """Without a process group each rank's result is its share; summed over
+    the ranks (as the all-reduce sums them) the loss and dW are the
+    full-batch ones and the dH rows tile the full dH. world > T leaves ranks
+    without positions: they contribute zeros."""
+    from oracle import kd_oracle as O
+
+    H, W, ids, logp = _inputs(T, 8, 24, 3, seed)
+    loss, dW, dH_rows = 0.0, 0.0, []
+    for r in range(world):
+        t0, t1 = dp.shard_range(T, world, r)
+        l, dH, dWr = dp.dp_fused_kl_step(torch.from_numpy(H[t0:t1]), torch.from_numpy(W), torch.from_numpy(ids[t0:t1]),
+                                         torch.from_numpy(logp[t0:t1]), 4, T, shard_call=oracle_shard_call,
+                                         grad_scale=gscale)
+        assert dH.shape == (t1 - t0, 8) and dWr.shape == W.shape
+        loss += float(l)
+        dW = dW + dWr.numpy()
+        dH_rows.append(dH.numpy())
+    loss_o, _, _ = O.fused_kl_forward(H, W, ids, logp)
+    dH_o, dW_o = O.fused_kl_backward(H, W, ids, logp, gscale / T)
+    assert abs(loss - loss_o) <= 1e-6 * abs(loss_o) + 1e-12
+    np.testing.assert_allclose(np.concatenate(dH_rows), dH_o, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(dW, dW_o, rtol=1e-12, atol=1e-15)

@@ -86,5 +86,18 @@ def test_one_rank_nccl_group_runs_the_collectives_on_the_device(cuda_dev):
         assert abs(lg.item() - l_full.item()) <= 1e-5 * abs(l_full.item())
         assert frob(Hg.grad.float().cpu().numpy(), 2.0 * dH_full.cpu().numpy()) <= 1e-2
         assert frob(Wg.grad.float().cpu().numpy(), 2.0 * dW_full.cpu().numpy()) <= 1e-2
+        # a rank without positions (more ranks than positions): zeros, no libkd
+        # call (libkd refuses T = 0), and both all-reduces still run
+        He, ide, lpe = H[:0], ids[:0], logp[:0]
+        loss_e, dH_e, dW_e = dp.dp_fused_kl_step(He, W, ide, lpe, 64, T, process_group=pg)
+        torch.cuda.synchronize()
+        assert loss_e.item() == 0.0 and dH_e.shape == (0, H.shape[1]) and dW_e.dtype == torch.float32
+        assert dW_e.device == W.device and not dW_e.any()
+        He_g = He.clone().requires_grad_(True)
+        We_g = W.clone().requires_grad_(True)
+        le = dp.DPFusedKL.apply(He_g, We_g, ide, lpe, 64, T, pg)
+        le.backward()
+        torch.cuda.synchronize()
+        assert le.item() == 0.0 and He_g.grad.shape == He.shape and not We_g.grad.any()
     finally:
         dist.destroy_process_group()

@@ -63,6 +63,17 @@ def libkd_shard_call(H, W, ids, logp, chunk: int, grad_scale: float, grad_scale_
     return ShardResult(loss * T, dH, dW)
 
 
+def _empty_shard(H, W) -> ShardResult:
+    """What a rank without positions contributes: no loss, no dH rows and a
+    zero dW (in the precision the loss would return it: fp32 for bf16, fp16
+    or fp32 weights). The loss itself is not called, since it refuses T = 0;
+    the rank still joins every collective."""
+    dW_dtype = torch.promote_types(W.dtype, torch.float32)
+    return ShardResult(torch.zeros((), dtype=torch.float64, device=W.device),
+                       torch.zeros((0, H.shape[1]), dtype=dW_dtype, device=H.device),
+                       torch.zeros(W.shape, dtype=dW_dtype, device=W.device))
+
+
 def _distributed() -> bool:
     """True when a default process group exists: the collectives then run
     (a one-rank group included)."""
@@ -83,7 +94,10 @@ def dp_fused_kl_step(H, W, ids, logp, chunk: int, T_global: int, shard_call: Sha
     shard's share of the global loss and gradient."""
     if T_global <= 0:
         raise ValueError("T_global must be positive")
-    r = shard_call(H, W, ids, logp, chunk, grad_scale / T_global)
+    if H.shape[0] == 0:  # more ranks than positions: this one has none
+        r = _empty_shard(H, W)
+    else:
+        r = shard_call(H, W, ids, logp, chunk, grad_scale / T_global)
     loss_sum = r.loss_sum.detach().reshape(1).to(torch.float64)
     dW = r.dW
     if _distributed():
@@ -100,12 +114,17 @@ class DPFusedKL(torch.autograd.Function):
     scalar all-reduce of the loss sum. Backward: libkd's recompute backward
     on the shard with the gradient scale 1 / T_global and the upstream
     gradient as a device scalar, then an all-reduce of dW; dH stays local.
-    Saves only the shard's lse (4 bytes per position)."""
+    Saves only the shard's lse (4 bytes per position). A rank whose shard is
+    empty contributes zeros and still joins both all-reduces."""
 
     @staticmethod
     def forward(ctx, H, W, ids, logp, chunk: int, T_global: int, process_group=None):
-        loss, lse, _ = fused_kl_fwd(H, W, ids, logp, chunk)
-        loss_sum = (loss.to(torch.float64) * H.shape[0]).reshape(1)
+        if H.shape[0] == 0:
+            lse = torch.zeros(0, dtype=torch.float32, device=H.device)
+            loss_sum = torch.zeros(1, dtype=torch.float64, device=H.device)
+        else:
+            loss, lse, _ = fused_kl_fwd(H, W, ids, logp, chunk)
+            loss_sum = (loss.to(torch.float64) * H.shape[0]).reshape(1)
         if _distributed():
             dist.all_reduce(loss_sum, op=dist.ReduceOp.SUM, group=process_group)
         ctx.save_for_backward(H, W, ids, logp, lse)
@@ -115,9 +134,12 @@ class DPFusedKL(torch.autograd.Function):
     @staticmethod
     def backward(ctx, g):
         H, W, ids, logp, lse = ctx.saved_tensors
-        g = g.detach().to(torch.float32).contiguous()
-        dH, dW = fused_kl_bwd(H, W, ids, logp, lse, ctx.chunk, 1.0 / ctx.T_global, grad_scale_dev=g,
-                              dH_bf16=H.dtype == torch.bfloat16)
+        if H.shape[0] == 0:
+            dH, dW = torch.zeros_like(H), torch.zeros(W.shape, dtype=torch.float32, device=W.device)
+        else:
+            g = g.detach().to(torch.float32).contiguous()
+            dH, dW = fused_kl_bwd(H, W, ids, logp, lse, ctx.chunk, 1.0 / ctx.T_global, grad_scale_dev=g,
+                                  dH_bf16=H.dtype == torch.bfloat16)
         if _distributed():
             dist.all_reduce(dW, op=dist.ReduceOp.SUM, group=ctx.pg)
         return dH, dW, None, None, None, None, None
