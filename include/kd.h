@@ -213,6 +213,9 @@ KD_API int kd_fused_kl_fwd(const void* H, const void* W, const int32_t* ids, con
  *   dH [T, d] float32 device, overwritten: dz W.
  *   dW [V, d] float32 device: dz^T H. It is added to the existing contents
  *      when accumulate_dW != 0, and overwritten otherwise.
+ *   Either of dH and dW may be NULL (not both): that gradient is then not
+ *   computed, and its GEMM (a quarter of the step's tensor work) is not
+ *   run. For a frozen LM head pass dW = NULL; for a frozen body, dH = NULL.
  *   lse        [T] float32 from kd_fused_kl_fwd on the same inputs.
  *   grad_scale host float s, and grad_scale_dev an optional device float32
  *              (NULL = 1) that multiplies s. The autograd binding passes
@@ -237,7 +240,8 @@ KD_API int kd_fused_kl_bwd(const void* H, const void* W, const int32_t* ids, con
  * the loss are those of [KD-TH] section "กลไก Fused Chunked KL Loss".
  * Outputs and arguments are those of kd_fused_kl_fwd followed by
  * kd_fused_kl_bwd (loss, lse and the optional loss_rows; dH overwritten,
- * dW overwritten or accumulated). The difference is that s = grad_scale
+ * dW overwritten or accumulated; either of dH and dW may be NULL, not
+ * both, to skip it). The difference is that s = grad_scale
  * (times *grad_scale_dev) must be known at call time. Results match the
  * two calls within rounding. dz off the teacher ids is rounded to bf16
  * twice (e, then dz), so it carries up to about 2^-8 relative error instead

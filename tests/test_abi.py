@@ -117,10 +117,16 @@ def test_fused_argument_errors(lib):
     bwd = lib.kd_fused_kl_bwd
     assert bwd(P16, P16, P16, P16, None, 64, 64, 128, 4, 32, 1.0, None, P16, P16, 0, ws, big, None) == \
         _native.KD_ERR_INVALID_ARG
-    assert bwd(P16, P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, None, P16, 0, ws, big, None) == \
+    # dH or dW may be NULL (that gradient is skipped), not both
+    assert bwd(P16, P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, None, None, 0, ws, big, None) == \
         _native.KD_ERR_INVALID_ARG
     assert bwd(P16, P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, ctypes.c_void_p(0x10004), P16, 0, ws,
                big, None) == _native.KD_ERR_UNSUPPORTED
+    assert bwd(P16, P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, P16, ctypes.c_void_p(0x10004), 0, ws,
+               big, None) == _native.KD_ERR_UNSUPPORTED
+    fb = lib.kd_fused_kl_fwdbwd
+    assert fb(P16, P16, P16, P16, 64, 64, 128, 4, 32, 1.0, None, P16, P16, None, None, None, 0, ws, big, None) == \
+        _native.KD_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("tau,over,bf", [(0.0, 0, 0), (-1.0, 0, 0), (float("inf"), 0, 0), (float("nan"), 0, 0),

@@ -203,24 +203,42 @@ def fused_kl_fwd(H, W, ids, logp, chunk: int, ws=None, want_rows: bool = False, 
     return loss, lse, rows
 
 
+def _grad_outputs(T, d, V, dev, dH, dW, dH_bf16, want_dH, want_dW):
+    """The dH / dW output tensors (allocated when not given), or None for a
+    gradient that is not wanted (libkd then skips its GEMM)."""
+    if not (want_dH or want_dW):
+        raise ValueError("want_dH and want_dW are both False: nothing to compute")
+    dh_dtype = torch.bfloat16 if dH_bf16 else torch.float32
+    if not want_dH:
+        dH = None
+    elif dH is None:
+        dH = torch.empty(T, d, dtype=dh_dtype, device=dev)
+    if not want_dW:
+        dW = None
+    elif dW is None:
+        dW = torch.empty(V, d, dtype=torch.float32, device=dev)
+    if dH is not None:
+        _need(dH, "dH", dh_dtype, dev)
+    if dW is not None:
+        _need(dW, "dW", torch.float32, dev)
+    return dH, dW
+
+
 def fused_kl_bwd(H, W, ids, logp, lse, chunk: int, grad_scale: float, grad_scale_dev=None, dH=None, dW=None,
                  accumulate_dW: bool = False, ws=None, temperature: float = 1.0, mask=None,
-                 mean_over_mask: bool = False, dH_bf16: bool = False, group: int = 0):
+                 mean_over_mask: bool = False, dH_bf16: bool = False, group: int = 0, want_dH: bool = True,
+                 want_dW: bool = True):
     """Backward: (dH [T, d] f32 (bf16 with dH_bf16), dW [V, d] f32) for
     dz = s (q - p); s = grad_scale * grad_scale_dev * 1/tau, times 1/N when
-    mean_over_mask (then grad_scale is d objective / d loss)."""
+    mean_over_mask (then grad_scale is d objective / d loss). want_dH /
+    want_dW = False skips that gradient (its GEMM does not run) and returns
+    None in its place."""
     T, d, V, K = _check_fused(H, W, ids, logp)
     dev = H.device
     _need(lse, "lse", torch.float32, dev)
     if ws is None:
         ws = fused_kl_workspace(d, V, K, chunk, dev, group)
-    dh_dtype = torch.bfloat16 if dH_bf16 else torch.float32
-    if dH is None:
-        dH = torch.empty(T, d, dtype=dh_dtype, device=dev)
-    if dW is None:
-        dW = torch.empty(V, d, dtype=torch.float32, device=dev)
-    _need(dH, "dH", dh_dtype, dev)
-    _need(dW, "dW", torch.float32, dev)
+    dH, dW = _grad_outputs(T, d, V, dev, dH, dW, dH_bf16, want_dH, want_dW)
     if grad_scale_dev is not None:
         _need(grad_scale_dev, "grad_scale_dev", torch.float32, dev)
     o, _m = _options(T, dev, temperature, mask, mean_over_mask, dH_bf16, group)
@@ -228,7 +246,7 @@ def fused_kl_bwd(H, W, ids, logp, lse, chunk: int, grad_scale: float, grad_scale
         "kd_fused_kl_bwd_ex",
         _native.lib().kd_fused_kl_bwd_ex(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(),
                                          lse.data_ptr(), T, d, V, K, chunk, float(grad_scale), _ptr(grad_scale_dev),
-                                         dH.data_ptr(), dW.data_ptr(), 1 if accumulate_dW else 0, _optp(o),
+                                         _ptr(dH), _ptr(dW), 1 if accumulate_dW else 0, _optp(o),
                                          ws.data_ptr(), ws.numel(), _stream_ptr(dev)),
     )
     return dH, dW
@@ -236,11 +254,12 @@ def fused_kl_bwd(H, W, ids, logp, lse, chunk: int, grad_scale: float, grad_scale
 
 def fused_kl_fwdbwd(H, W, ids, logp, chunk: int, grad_scale: float | None = None, grad_scale_dev=None, dH=None,
                     dW=None, accumulate_dW: bool = False, ws=None, want_rows: bool = False, temperature: float = 1.0,
-                    mask=None, mean_over_mask: bool = False, dH_bf16: bool = False, group: int = 0):
+                    mask=None, mean_over_mask: bool = False, dH_bf16: bool = False, group: int = 0,
+                    want_dH: bool = True, want_dW: bool = True):
     """Forward and backward in one call, without recomputing the logits:
     (loss, lse, loss_rows or None, dH, dW). grad_scale defaults to the
     gradient of the loss itself: 1/T, or 1 with mean_over_mask (the library
-    then applies 1/N)."""
+    then applies 1/N). want_dH / want_dW as in fused_kl_bwd."""
     T, d, V, K = _check_fused(H, W, ids, logp)
     dev = H.device
     if ws is None:
@@ -250,13 +269,7 @@ def fused_kl_fwdbwd(H, W, ids, logp, chunk: int, grad_scale: float | None = None
     loss = torch.empty((), dtype=torch.float32, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
     rows = torch.empty(T, dtype=torch.float32, device=dev) if want_rows else None
-    dh_dtype = torch.bfloat16 if dH_bf16 else torch.float32
-    if dH is None:
-        dH = torch.empty(T, d, dtype=dh_dtype, device=dev)
-    if dW is None:
-        dW = torch.empty(V, d, dtype=torch.float32, device=dev)
-    _need(dH, "dH", dh_dtype, dev)
-    _need(dW, "dW", torch.float32, dev)
+    dH, dW = _grad_outputs(T, d, V, dev, dH, dW, dH_bf16, want_dH, want_dW)
     if grad_scale_dev is not None:
         _need(grad_scale_dev, "grad_scale_dev", torch.float32, dev)
     o, _m = _options(T, dev, temperature, mask, mean_over_mask, dH_bf16, group)
@@ -264,7 +277,7 @@ def fused_kl_fwdbwd(H, W, ids, logp, chunk: int, grad_scale: float | None = None
         "kd_fused_kl_fwdbwd_ex",
         _native.lib().kd_fused_kl_fwdbwd_ex(H.data_ptr(), W.data_ptr(), ids.data_ptr(), logp.data_ptr(), T, d, V, K,
                                             chunk, float(grad_scale), _ptr(grad_scale_dev), loss.data_ptr(),
-                                            lse.data_ptr(), _ptr(rows), dH.data_ptr(), dW.data_ptr(),
+                                            lse.data_ptr(), _ptr(rows), _ptr(dH), _ptr(dW),
                                             1 if accumulate_dW else 0, _optp(o), ws.data_ptr(), ws.numel(),
                                             _stream_ptr(dev)),
     )
@@ -278,7 +291,9 @@ class FusedKL(torch.autograd.Function):
     mean_over_mask=False, group=0). Forward saves only lse [T] (4 bytes per
     position). Backward recomputes each chunk's logits. The upstream gradient
     goes to the kernels as a device scalar, so backward does not synchronise.
-    dH comes out of the kernels in H's dtype when H is bf16.
+    dH comes out of the kernels in H's dtype when H is bf16. Only the
+    gradients autograd asks for are computed: with a frozen LM head
+    (W.requires_grad False) the dW GEMM does not run.
     """
 
     @staticmethod
@@ -295,10 +310,13 @@ class FusedKL(torch.autograd.Function):
     @staticmethod
     def backward(ctx, g):
         H, W, ids, logp, lse = ctx.saved_tensors
+        want_dH, want_dW = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        if not (want_dH or want_dW):
+            return None, None, None, None, None, None, None, None, None
         g = g.detach().to(torch.float32).contiguous()
         over_mask = bool(ctx.mean_over_mask) and ctx.mask is not None
         dH, dW = fused_kl_bwd(H, W, ids, logp, lse, ctx.chunk, 1.0 if over_mask else 1.0 / H.shape[0],
                               grad_scale_dev=g, ws=ctx.ws, temperature=ctx.temperature, mask=ctx.mask,
                               mean_over_mask=ctx.mean_over_mask, dH_bf16=H.dtype == torch.bfloat16,
-                              group=ctx.group)
+                              group=ctx.group, want_dH=want_dH, want_dW=want_dW)
         return dH, dW, None, None, None, None, None, None, None

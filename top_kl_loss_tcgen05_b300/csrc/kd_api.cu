@@ -292,10 +292,11 @@ namespace {
 //   dH_g^T = W^T dz^T (stored transposed into dH) and
 //   dW (+)= dz^T H_g.
 // `ag` carries the tensor maps of W (tmA[0]) and dW (tmC[1]) set up once
-// per call.
+// per call. Either output may be absent (dH == NULL, or want_dW == 0): its
+// problem then has no tiles (no dW also means no H_g^T).
 int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __nv_bfloat16* dz,
-               __nv_bfloat16* hct, void* dH, int dH_bf16, int64_t g0, int grows, int64_t d, int64_t V,
-               int reduce_add, int sms, cudaStream_t s) {
+               __nv_bfloat16* hct, void* dH, int dH_bf16, int want_dW, int64_t g0, int grows, int64_t d,
+               int64_t V, int reduce_add, int sms, cudaStream_t s) {
   const int TR = gemm_tile_rows(ag.cta2), BR = gemm_b_box_rows(ag.cta2);
   // dW's N runs over d. With wide pair tiles and d a multiple of 480 but not
   // of 512 (d = 2880 at the GPT-OSS shapes), 480-wide tiles (two N = 240
@@ -303,17 +304,18 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
   // padding.
   const bool dw480 = ag.cta2 && ag.wide && d % 512 != 0 && d % 480 == 0;
   cudaError_t e;
-  {
+  if (want_dW) {
     ProfScope ps(K_TRANSPOSE, s);
     e = launch_transpose(Hb + g0 * d, grows, (int)d, hct, (int)L.ldt, s);
+    if (e != cudaSuccess) return cuda_status(e);
   }
-  if (e != cudaSuccess) return cuda_status(e);
   const cudaError_t eh =
-      dH_bf16 ? encode_map_2d_plain(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                                    static_cast<__nv_bfloat16*>(dH) + g0 * d, (uint64_t)d, (uint64_t)grows,
-                                    (uint64_t)d * 2, 32, 32)
-              : encode_map_2d(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, static_cast<float*>(dH) + g0 * d,
-                              (uint64_t)d, (uint64_t)grows, (uint64_t)d * 4, 32, 32);
+      !dH ? cudaSuccess
+      : dH_bf16 ? encode_map_2d_plain(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                      static_cast<__nv_bfloat16*>(dH) + g0 * d, (uint64_t)d, (uint64_t)grows,
+                                      (uint64_t)d * 2, 32, 32)
+                : encode_map_2d(&ag.tmC[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, static_cast<float*>(dH) + g0 * d,
+                                (uint64_t)d, (uint64_t)grows, (uint64_t)d * 4, 32, 32);
   if (eh != cudaSuccess ||
       encode_map_2d(&ag.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dz, (uint64_t)V, (uint64_t)grows,
                     (uint64_t)L.ldz * 2, kBK, BR) != cudaSuccess ||
@@ -323,7 +325,7 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
                     (uint64_t)L.ldt * 2, kBK, dw480 ? 120 : BR) != cudaSuccess)
     return KD_ERR_UNSUPPORTED;
   Problem& P0 = ag.pr[0];
-  P0.m_blocks = (int)ceil_div(d, TR);
+  P0.m_blocks = dH ? (int)ceil_div(d, TR) : 0;  // no dH: no tiles of this problem
   P0.n_blocks = (int)ceil_div(grows, gemm_tile_cols(ag.cta2, ag.wide));
   P0.k_blocks = (int)ceil_div(V, kBK);
   P0.a_mn = 1; P0.b_mn = 0; P0.M = (int)d; P0.N = grows;
@@ -338,8 +340,8 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
   P1.tile_begin = P0.m_blocks * P0.n_blocks; P1.n_fastest = 1;
   P1.reduce_add = reduce_add;
   P1.c_trans = 0; P1.out_bf16 = 0;
-  ag.nprob = 2;
-  ag.total_tiles = P1.tile_begin + P1.m_blocks * P1.n_blocks;
+  ag.nprob = want_dW ? 2 : 1;
+  ag.total_tiles = want_dW ? P1.tile_begin + P1.m_blocks * P1.n_blocks : P1.tile_begin;
   {
     ProfScope ps(K_GRAD, s);
     e = launch_grad(ag, sms, s);
@@ -348,7 +350,7 @@ int grad_group(GemmArgs& ag, const Layout& L, const __nv_bfloat16* Hb, const __n
 }
 
 // Tensor maps of W (M-major A of the dH^T problem) and dW (C of the dW
-// problem), shared by every group of a call.
+// problem; none when dW is not wanted), shared by every group of a call.
 int grad_setup(GemmArgs& ag, const void* W, float* dW, int64_t d, int64_t V, int* status, int* counter) {
   std::memset(&ag, 0, sizeof(ag));
   ag.cta2 = gemm_cta2();
@@ -356,11 +358,12 @@ int grad_setup(GemmArgs& ag, const void* W, float* dW, int64_t d, int64_t V, int
   ag.status = status;
   ag.tile_counter = counter;
   if (encode_map_2d(&ag.tmA[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)d, (uint64_t)V, (uint64_t)d * 2, 64,
-                    64) != cudaSuccess ||
-      encode_map_2d(&ag.tmC[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, (uint64_t)d, (uint64_t)V, (uint64_t)d * 4, 32,
-                    32) != cudaSuccess ||
-      encode_map_2d_plain(&ag.tmCt[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, (uint64_t)d, (uint64_t)V,
-                          (uint64_t)d * 4, 16, 32) != cudaSuccess)
+                    64) != cudaSuccess)
+    return KD_ERR_UNSUPPORTED;
+  if (dW && (encode_map_2d(&ag.tmC[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, (uint64_t)d, (uint64_t)V, (uint64_t)d * 4,
+                           32, 32) != cudaSuccess ||
+             encode_map_2d_plain(&ag.tmCt[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, (uint64_t)d, (uint64_t)V,
+                                 (uint64_t)d * 4, 16, 32) != cudaSuccess))
     return KD_ERR_UNSUPPORTED;
   return KD_OK;
 }
@@ -620,8 +623,8 @@ int kd_fused_kl_bwd_ex(const void* H, const void* W, const int32_t* ids, const f
   if (st != KD_OK) return st;
   st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, o.group, ws, ws_bytes);
   if (st != KD_OK) return st;
-  if (!lse || !dH || !dW) return KD_ERR_INVALID_ARG;
-  if (!aligned(dH, 16) || !aligned(dW, 16)) return KD_ERR_UNSUPPORTED;
+  if (!lse || (!dH && !dW)) return KD_ERR_INVALID_ARG;
+  if ((dH && !aligned(dH, 16)) || (dW && !aligned(dW, 16))) return KD_ERR_UNSUPPORTED;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -657,7 +660,8 @@ int kd_fused_kl_bwd_ex(const void* H, const void* W, const int32_t* ids, const f
       e = launch_logits_dz(az, sms, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
-    st = grad_group(ag, L, Hb, f.dz, f.hct, dH, o.dH_bf16, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms,
+    st = grad_group(ag, L, Hb, f.dz, f.hct, dH, o.dH_bf16, dW != nullptr, g0, grows, d, V,
+                    (accumulate_dW || g0 > 0) ? 1 : 0, sms,
                     s);
     if (st != KD_OK) return st;
   }
@@ -682,8 +686,8 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
   if (st != KD_OK) return st;
   st = check_fused_args(H, W, ids, logp, T, d, V, K, chunk, o.group, ws, ws_bytes);
   if (st != KD_OK) return st;
-  if (!loss || !lse || !dH || !dW) return KD_ERR_INVALID_ARG;
-  if (!aligned(dH, 16) || !aligned(dW, 16)) return KD_ERR_UNSUPPORTED;
+  if (!loss || !lse || (!dH && !dW)) return KD_ERR_INVALID_ARG;
+  if ((dH && !aligned(dH, 16)) || (dW && !aligned(dW, 16))) return KD_ERR_UNSUPPORTED;
   const int sms = num_sms_current();
   if (sms <= 0) return KD_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -728,7 +732,8 @@ int kd_fused_kl_fwdbwd_ex(const void* H, const void* W, const int32_t* ids, cons
                              f.zK, f.cnt, L.Kp, 1.f, f.scale, mask_at(o, g0), s);
     }
     if (e != cudaSuccess) return cuda_status(e);
-    st = grad_group(ag, L, Hb, f.dz, f.hct, dH, o.dH_bf16, g0, grows, d, V, (accumulate_dW || g0 > 0) ? 1 : 0, sms,
+    st = grad_group(ag, L, Hb, f.dz, f.hct, dH, o.dH_bf16, dW != nullptr, g0, grows, d, V,
+                    (accumulate_dW || g0 > 0) ? 1 : 0, sms,
                     s);
     if (st != KD_OK) return st;
   }

@@ -114,8 +114,10 @@ class DPFusedKL(torch.autograd.Function):
     scalar all-reduce of the loss sum. Backward: libkd's recompute backward
     on the shard with the gradient scale 1 / T_global and the upstream
     gradient as a device scalar, then an all-reduce of dW; dH stays local.
-    Saves only the shard's lse (4 bytes per position). A rank whose shard is
-    empty contributes zeros and still joins both all-reduces."""
+    Only the gradients autograd asks for are computed (a frozen LM head
+    skips the dW GEMM and its all-reduce, on every rank alike). Saves only
+    the shard's lse (4 bytes per position). A rank whose shard is empty
+    contributes zeros and still joins both all-reduces."""
 
     @staticmethod
     def forward(ctx, H, W, ids, logp, chunk: int, T_global: int, process_group=None):
@@ -134,12 +136,16 @@ class DPFusedKL(torch.autograd.Function):
     @staticmethod
     def backward(ctx, g):
         H, W, ids, logp, lse = ctx.saved_tensors
+        want_dH, want_dW = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        if not (want_dH or want_dW):
+            return None, None, None, None, None, None, None
         if H.shape[0] == 0:
-            dH, dW = torch.zeros_like(H), torch.zeros(W.shape, dtype=torch.float32, device=W.device)
+            dH = torch.zeros_like(H) if want_dH else None
+            dW = torch.zeros(W.shape, dtype=torch.float32, device=W.device) if want_dW else None
         else:
             g = g.detach().to(torch.float32).contiguous()
             dH, dW = fused_kl_bwd(H, W, ids, logp, lse, ctx.chunk, 1.0 / ctx.T_global, grad_scale_dev=g,
-                                  dH_bf16=H.dtype == torch.bfloat16)
-        if _distributed():
+                                  dH_bf16=H.dtype == torch.bfloat16, want_dH=want_dH, want_dW=want_dW)
+        if want_dW and _distributed():
             dist.all_reduce(dW, op=dist.ReduceOp.SUM, group=ctx.pg)
         return dH, dW, None, None, None, None, None
