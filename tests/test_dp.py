@@ -145,3 +145,19 @@ def test_shards_of_any_split_sum_to_the_full_batch(T, world, gscale, seed):
     assert abs(loss - loss_o) <= 1e-6 * abs(loss_o) + 1e-12
     np.testing.assert_allclose(np.concatenate(dH_rows), dH_o, rtol=1e-12, atol=1e-15)
     np.testing.assert_allclose(dW, dW_o, rtol=1e-12, atol=1e-15)
+
+
+def test_empty_shard_gives_zeros_in_the_loss_precision_without_calling_the_loss():
+    """bf16 weights (as libkd takes them): the empty shard's dW is fp32, the
+    precision libkd returns dW in, so every rank all-reduces the same dtype."""
+    def must_not_run(*a, **k):
+        raise AssertionError("the loss was called on an empty shard")
+
+    H = torch.zeros(0, 16, dtype=torch.bfloat16)
+    W = torch.randn(40, 16).to(torch.bfloat16)
+    ids, logp = torch.zeros(0, 4, dtype=torch.int32), torch.zeros(0, 4)
+    loss, dH, dW = dp.dp_fused_kl_step(H, W, ids, logp, 8, 100, shard_call=must_not_run)
+    assert float(loss) == 0.0 and dH.shape == (0, 16)
+    assert dW.dtype == torch.float32 and dW.shape == (40, 16) and not dW.any()
+    with pytest.raises(ValueError):
+        dp.dp_fused_kl_step(H, W, ids, logp, 8, 0, shard_call=must_not_run)
